@@ -1,0 +1,393 @@
+"""Benchmark of the fused GEMM + epilogue path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the large linear-layer pair at fp16 with fp32 accumulation --
+  forward  RELU_AUX_BIAS  Y = ReLU(X W + bias), relu_aux    X[65536,16384] W[16384,8192]
+  backward DRELU_BGRAD    dZ = (dY W^T) masked, bgrad      dY[65536,8192], mask [65536,16384]
+(the fp16 (65536,16384) x (16384,8192) workload of "Fusing Matmul Epilogs
+with nvmath-python", section "Suitable evaluation scenarios"). Inputs are
+seeded synthetic draws (synth) already resident in HBM; every operand is far
+larger than L2, so no flush is needed between steps.
+
+Prints one JSON line: throughput in TFLOP/s (2*M*N*K per GEMM), % of the
+dense fp16/bf16 peak, the dominant kernel's roofline, the CPU oracle as a
+timed baseline, an end-to-end figure through the C ABI from pinned host
+buffers, and the epilogue's overhead against the same kernel with no
+epilogue. ``--impl reference`` times the CPU oracle on the same workload.
+Several GPUs run independent replicas (the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+M, K, N = 65536, 16384, 8192  # forward X[M,K] . W[K,N]; backward dY[M,N] . W^T -> [M,K]
+WORKLOAD = "linear_pair_fp16_fwd_relu_aux_bias_bwd_drelu_bgrad_65536x16384x8192"
+METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 FP16/BF16 dense peak, 1 GPU"
+FLOP_PER_GEMM = 2.0 * M * N * K
+FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- CPU oracle leg
+def oracle_sample(rows_fwd: int, rows_bwd: int, nthreads: int):
+    """Run the CPU oracle on `rows` sampled rows of both GEMMs of one step.
+    Returns (flops done, seconds of oracle work, description)."""
+    import oracle
+    t_gen0 = time.time()
+    W = synth.normal((K, N), synth.F16, 0, synth.TID_B, 1 / 128)
+    bias = synth.normal((N,), synth.F16, 0, synth.TID_BIAS, 0.1)
+    rows = synth.sample_rows(M, 64, 0)
+    rf, rb = rows[:rows_fwd], rows[:rows_bwd]
+    X = synth.normal((M, K), synth.F16, 0, synth.TID_A, 1.0, rows=rf)
+    dY = synth.normal((M, N), synth.F16, 0, synth.TID_DY, 1.0, rows=rb)
+    words = synth.mask_words(M, K, 0)  # Bernoulli(1/2) mask of the backward, [M/32, K]
+    gen_s = time.time() - t_gen0
+    t0 = time.time()
+    oracle.relu_bias(X, W, bias, oracle.F16, oracle.B_KN, oracle.BIAS_COL, row_ids=rf,
+                     nthreads=nthreads)
+    # backward: dY . W^T, W [K, N] being the [n, k] storage of B = W^T
+    oracle.drelu_bgrad(dY, W, words, oracle.F16, oracle.B_NK, row_ids=rb, nthreads=nthreads)
+    sec = time.time() - t0
+    flops = 2.0 * len(rf) * N * K + 2.0 * len(rb) * K * N
+    desc = (f"{len(rf)} sampled rows of the forward and {len(rb)} of the backward GEMM + epilogue "
+            f"(full N, full K), {nthreads} threads; input generation {gen_s:.1f}s not timed")
+    return flops, sec, desc
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    nthreads = os.cpu_count() or 1
+    per_step_rows = max(1, args.ref_rows)
+    for _ in range(args.warmup):
+        oracle_sample(1, 1, nthreads)
+    times, flops_tot = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        fl, sec, desc = oracle_sample(per_step_rows, per_step_rows, nthreads)
+        times.append(sec)
+        flops_tot += fl
+    total = sum(times)
+    value = flops_tot / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------- GPU leg
+def run_gpu(args):
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gf.build()
+    synth.build_cuda()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    f16 = torch.float16
+    X = torch.empty((M, K), dtype=f16, device=dev)
+    W = torch.empty((K, N), dtype=f16, device=dev)
+    bias = torch.empty((N,), dtype=f16, device=dev)
+    dY = torch.empty((M, N), dtype=f16, device=dev)
+    mask = torch.empty((M // 32, K), dtype=torch.int32, device=dev)
+    Y = torch.empty((M, N), dtype=f16, device=dev)
+    aux = torch.empty((M // 32, N), dtype=torch.int32, device=dev)
+    dZ = torch.empty((M, K), dtype=f16, device=dev)
+    bgrad = torch.empty((K,), dtype=torch.float32, device=dev)
+    seed = 0
+    synth.dev_normal(X, synth.F16, seed, synth.TID_A, 1.0, sp)
+    synth.dev_normal(W, synth.F16, seed, synth.TID_B, 1 / 128, sp)
+    synth.dev_normal(bias, synth.F16, seed, synth.TID_BIAS, 0.1, sp)
+    synth.dev_normal(dY, synth.F16, seed, synth.TID_DY, 1.0, sp)
+    synth.dev_mask_words(mask, M, K, seed, synth.TID_MASK, sp)
+    torch.cuda.synchronize()
+
+    fwd = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL,
+                               gf.GF_B_KN)
+    bwd = gf.gf_matmul_plan_ex(M, K, N, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                               gf.GF_B_NK)
+    fwd_none = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
+                                    gf.GF_B_KN)
+    bwd_none = gf.gf_matmul_plan_ex(M, K, N, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
+                                    gf.GF_B_NK)
+    launches_per_step = 3  # fused forward, fused backward, bgrad finalize
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        gf.gf_matmul_execute(fwd, X, W, bias=bias, out=Y, aux_out=aux, stream=sp)
+        if ev is not None:
+            ev[1].record(stream)
+        gf.gf_matmul_execute(bwd, dY, W, out=dZ, aux_in=mask, bgrad=bgrad, stream=sp)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    assert gf.gf_plan_status(fwd, sp) == gf.GF_OK and gf.gf_plan_status(bwd, sp) == gf.GF_OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    barrier()
+    clk = clocks.stop()
+    status_ok = gf.gf_plan_status(fwd, sp) == gf.GF_OK and gf.gf_plan_status(bwd, sp) == gf.GF_OK
+    ms_total = t_start.elapsed_time(t_end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+
+    # epilogue overhead: the same kernels and tiles with no epilogue
+    def time_plan(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(2, min(args.steps, 5))
+    t_fwd_none = time_plan(lambda: gf.gf_matmul_execute(fwd_none, X, W, out=Y, stream=sp), reps)
+    t_fwd_epi = time_plan(lambda: gf.gf_matmul_execute(fwd, X, W, bias=bias, out=Y, aux_out=aux,
+                                                       stream=sp), reps)
+    t_bwd_none = time_plan(lambda: gf.gf_matmul_execute(bwd_none, dY, W, out=dZ, stream=sp), reps)
+    t_bwd_epi = time_plan(lambda: gf.gf_matmul_execute(bwd, dY, W, out=dZ, aux_in=mask,
+                                                       bgrad=bgrad, stream=sp), reps)
+
+    # end to end through the C ABI from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                   for n, t in (("X", X), ("W", W), ("bias", bias), ("dY", dY), ("mask", mask))}
+        for n, t in (("X", X), ("W", W), ("bias", bias), ("dY", dY), ("mask", mask)):
+            host_in[n].copy_(t)
+        host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for n, t in (("Y", Y), ("aux", aux), ("dZ", dZ), ("bgrad", bgrad))}
+        dev_in = {"X": X, "W": W, "bias": bias, "dY": dY, "mask": mask}
+        dev_out = {"Y": Y, "aux": aux, "dZ": dZ, "bgrad": bgrad}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n, t in dev_in.items():
+                t.copy_(host_in[n], non_blocking=True)
+            step()
+            for n, t in dev_out.items():
+                host_out[n].copy_(t, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e2e_steps = max(1, min(args.steps, 3))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e2e_ms = a.elapsed_time(b) / e2e_steps
+        e2e = {"value": world * 2 * FLOP_PER_GEMM / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del host_in, host_out
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        return 0
+
+    pk, pk_kind = peaks()
+    ms_step = ms_total / args.steps
+    value = world * 2 * FLOP_PER_GEMM / (ms_step * 1e-3) / 1e12
+    fwd_avg, bwd_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    dom_name, dom_ms = ("fused forward RELU_AUX_BIAS", fwd_avg) if fwd_avg >= bwd_avg else \
+        ("fused backward DRELU_BGRAD (+ finalize)", bwd_avg)
+    peak_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in pk else "bf16_tflops"
+    peak = float(pk[peak_key])
+    achieved = FLOP_PER_GEMM / (dom_ms * 1e-3) / 1e12
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        fl, sec, desc = oracle_sample(args.ref_rows, args.ref_rows, nthreads)
+        cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+               "sample": desc, "seconds": sec}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "seed": 0,
+                   "l2": "inputs larger than L2 (X 2.1 GB, dY 1.1 GB); no flush",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": {"value": 100 * value / world / peak, "peak_tflops": peak,
+                        "peak_kind": f"{pk_kind} {peak_key}",
+                        "vs_nominal_2250": 100 * value / world / 2250.0},
+        "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{pk_kind} {peak_key}",
+                     "algorithmic_flop_per_launch": FLOP_PER_GEMM},
+        "kernels_ms": {"fwd_relu_aux_bias": fwd_avg, "bwd_drelu_bgrad": bwd_avg,
+                       "fwd_none": t_fwd_none, "bwd_none": t_bwd_none,
+                       "fwd_epi_isolated": t_fwd_epi, "bwd_epi_isolated": t_bwd_epi},
+        "epilogue_overhead": {"fwd": t_fwd_epi / t_fwd_none - 1, "bwd": t_bwd_epi / t_bwd_none - 1},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "status_ok": status_ok,
+    }
+    print(json.dumps(line), flush=True)
+    for p in (fwd, bwd, fwd_none, bwd_none):
+        p.free()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gf", choices=["gf", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=8,
+                    help="sampled rows per GEMM in each CPU-oracle sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "gf":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,423 @@
+// Persistent, warp-specialised fused GEMM + epilogue kernel for sm_103a.
+//
+//   warp 0      : TMA producer -- loads A and B k-slices into a ring of
+//                 shared-memory stages (128-byte swizzle, no multicast).
+//   warp 1      : allocates tensor memory and issues tcgen05.mma (one thread)
+//                 into a double-buffered fp32 accumulator in TMEM.
+//   warps 2..5  : epilogue -- drain TMEM with tcgen05.ld (warp w reads TMEM
+//                 lanes 32*(w%4)..+31, i.e. 32 rows of the tile), apply the
+//                 epilog and store. The second accumulator buffer lets the
+//                 epilogue of tile t run under the mainloop of tile t+1.
+//
+// Epilogs (web pages on fused matmul epilogs: "Fusing Matmul Epilogs with
+// nvmath-python", sections "The problem addressed by fused epilogs",
+// "Forward-pass capabilities in the source", "Backward-pass path shown in the
+// example"; nvmath-python / cuBLASLt page, step 2 and "other epilogs"):
+//   NONE          out = acc
+//   BIAS          out = acc + bias
+//   RELU_BIAS     out = max(acc + bias, 0)
+//   RELU_AUX_BIAS RELU_BIAS, plus the ReLU mask (z > 0) packed with
+//                 __ballot_sync into column words: a warp's 32 lanes are 32
+//                 consecutive rows, so one ballot is one word.
+//   DRELU_BGRAD   dz = acc where the mask bit is set, else 0; out = dz; the
+//                 column sums of dz are reduced in the CTA (warp shuffles,
+//                 then the four warps in a fixed order) and written as one
+//                 partial per tile, or added with one atomicAdd per column.
+//
+// Every mbarrier wait is bounded; on time-out the kernel records an error in
+// the plan's status word, tells the other roles to stop, waits for its own
+// copies and MMAs in flight and frees its tensor memory before returning.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace gf {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // 64 x 16-bit = 128 bytes = one swizzle row
+constexpr int kThreads = 192;
+
+template <int BN>
+struct TileCfg {
+  static_assert(BN == 128 || BN == 256, "tile N");
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+  static constexpr int kCtrlBytes = 1024;
+  static constexpr int kRedBytes = 4 * BN * 4;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * (kABytes + kBBytes) +
+                                    kCtrlBytes + kRedBytes;
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<__half>(__half x) {
+  return __half2float(x);
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 8 consecutive 16-bit values -> fp32
+template <typename T>
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  const T* h = reinterpret_cast<const T*>(&u);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[i] = to_f32<T>(h[i]);
+}
+
+// Tile t -> (m block, n block): groups of group_m row blocks are swept
+// column by column so that CTAs running together share A and B in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+  const int group_size = p.group_m * p.num_n_blocks;
+  const int group = t / group_size;
+  const int first_m = group * p.group_m;
+  const int gm = min(p.num_m_blocks - first_m, p.group_m);
+  const int r = t - group * group_size;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* abort_flag,
+                                            int code) {
+  *abort_flag = 1;
+  atomicOr(p.status, code);
+}
+
+template <int EPI, typename T, bool B_MN, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_epilog_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using C = TileCfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + S * C::kABytes;
+  const uint32_t ctrl = sB + S * C::kBBytes;
+  uint8_t* gctrl = gbase + (ctrl - base);
+  const uint32_t full0 = ctrl;               // S barriers: stage filled
+  const uint32_t empty0 = ctrl + 8u * S;     // S barriers: stage consumed
+  const uint32_t tfull0 = ctrl + 16u * S;    // 2 barriers: accumulator ready
+  const uint32_t tempty0 = tfull0 + 16u;     // 2 barriers: accumulator drained
+  const uint32_t done_bar = tempty0 + 16u;   // MMA teardown
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gctrl + 16 * S + 40);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 44);
+  float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);  // [4][BN]
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(tfull0, 1);
+    mbar_init(tfull0 + 8u, 1);
+    mbar_init(tempty0, 4);
+    mbar_init(tempty0 + 8u, 4);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (p.num_k_blocks > 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && p.num_k_blocks > 0) {
+      int issued[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) issued[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int loads = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, t, mb, nb);
+        const int m0 = mb * kBM, n0 = nb * BN;
+        const int nbox = B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 1;
+        const uint32_t bytes = C::kABytes + (B_MN ? nbox * 64 * kBK * 2 : C::kBBytes);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          ++loads;
+          if (loads != p.drop_load) {
+            const uint32_t fb = full0 + 8u * stage;
+            mbar_arrive_expect_tx(fb, bytes);
+            tma_load_2d(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0);
+            if (B_MN) {
+              for (int j = 0; j < nbox; ++j)
+                tma_load_2d(sB + stage * C::kBBytes + j * (64 * kBK * 2), &tmB, fb, n0 + 64 * j,
+                            kb * kBK);
+            } else {
+              tma_load_2d(sB + stage * C::kBBytes, &tmB, fb, kb * kBK, n0);
+            }
+            issued[stage] = (int)phase;
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // every load issued must land before the CTA may exit
+#pragma unroll
+      for (int s = 0; s < S; ++s)
+        if (issued[s] >= 0 &&
+            !mbar_wait_bounded(full0 + 8u * s, (uint32_t)issued[s], nullptr, p.wait_limit_ns))
+          raise_error(p, abort_flag, ST_TIMEOUT_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(kBf16, B_MN, kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_bounded(tempty0 + 8u * buf, use ^ 1u, abort_flag, p.wait_limit_ns)) {
+          raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        if (p.num_k_blocks == 0) {
+          mbar_arrive(tfull0 + 8u * buf);  // acc is all zeros: nothing to multiply
+          continue;
+        }
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = sA + stage * C::kABytes;
+          const uint32_t b_base = sB + stage * C::kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K-major A: 16 k = 32 bytes along the swizzled 128-byte row;
+            // 8-row groups 1024 bytes apart.
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            // B K-major: as A. B MN-major: 16 k = 16 rows of 128 bytes;
+            // 64-column chunks 64*128 bytes apart (LBO), 8-k groups 1024 (SBO).
+            const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
+                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8u * stage);  // frees the stage once these MMAs finish
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit(tfull0 + 8u * buf);
+      }
+      // all MMAs issued by this thread must finish before TMEM is freed
+      umma_commit(done_bar);
+      if (!mbar_wait_bounded(done_bar, 0, nullptr, p.wait_limit_ns))
+        raise_error(p, abort_flag, ST_TIMEOUT_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // the TMEM lane quarter this warp may access
+    const int ep_tid = threadIdx.x - 64;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
+      if constexpr (EPI == EPI_DRELU_BGRAD) {
+        // the four warps meet at named barriers below: they must agree
+        ok = !named_bar_red_or(1, 128, !ok);
+      }
+      if (!ok) {
+        raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      int mb, nb;
+      tile_coords(p, t, mb, nb);
+      const int m0 = mb * kBM, n0 = nb * BN;
+      const int row = m0 + 32 * q + (int)lane;
+      const bool row_ok = row < p.M;
+      const int wrow = (m0 >> 5) + q;  // relu_aux word row of this warp's 32 rows
+      const bool wrow_ok = m0 + 32 * q < p.M;
+      const T* bias = reinterpret_cast<const T*>(p.bias);
+      float row_bias = 0.f;
+      if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS || EPI == EPI_BIAS) {
+        if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
+      }
+      T* out = reinterpret_cast<T*>(p.out);
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN);
+
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + 32 * c;
+        if (col0 >= p.N) break;  // same for every epilogue warp
+        float v[32];
+        if (p.num_k_blocks > 0) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + 32u * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+
+        if constexpr (EPI == EPI_DRELU_BGRAD) {
+          uint32_t my_word = 0;
+          if (wrow_ok && col0 + (int)lane < p.N)
+            my_word = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t w = __shfl_sync(0xFFFFFFFFu, my_word, j);
+            v[j] = ((w >> lane) & 1u) ? v[j] : 0.f;
+          }
+        } else if constexpr (EPI != EPI_NONE) {
+          if (p.bias_axis == 0) {
+            const T* bp = bias + col0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              float b8[8];
+              if (col0 + 8 * g < p.N) {
+                unpack8<T>(__ldg(reinterpret_cast<const uint4*>(bp + 8 * g)), b8);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) b8[i] = 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] + b8[i];
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = v[j] + row_bias;
+          }
+          if constexpr (EPI == EPI_RELU_AUX_BIAS) {
+            uint32_t my_word = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_ok && v[j] > 0.f);
+              my_word = (lane == (uint32_t)j) ? bal : my_word;
+            }
+            if (wrow_ok && col0 + (int)lane < p.N)
+              p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
+          }
+          if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
+          }
+        }
+
+        if (row_ok) {
+          T* op = out + (size_t)row * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + 8 * g < p.N) {
+              uint4 u;
+              u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
+              u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
+              u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
+              u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
+              *reinterpret_cast<uint4*>(op + 8 * g) = u;
+            }
+          }
+        }
+
+        if constexpr (EPI == EPI_DRELU_BGRAD) {
+          // transpose-reduce: after 5 halving steps (31 shuffles) lane l
+          // holds the sum of column col0 + l over this warp's 32 rows
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) {
+            const bool upper = (lane & (uint32_t)o) != 0;
+#pragma unroll
+            for (int i = 0; i < o; ++i) {
+              const float send = upper ? v[i] : v[i + o];
+              const float keep = upper ? v[i + o] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+            }
+          }
+          red[q * BN + 32 * c + (int)lane] = v[0];
+        }
+      }
+      // accumulator buffer drained: the MMA warp may reuse it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8u * buf);
+
+      if constexpr (EPI == EPI_DRELU_BGRAD) {
+        named_bar_sync(1, 128);
+        for (int col = ep_tid; col < BN; col += 128) {
+          if (n0 + col < p.N) {
+            // the four warps' 32-row sums, always in the same order
+            const float s = ((red[col] + red[BN + col]) + red[2 * BN + col]) + red[3 * BN + col];
+            if (p.bgrad_atomic)
+              atomicAdd(p.bgrad + n0 + col, s);
+            else
+              p.bgrad[(size_t)mb * p.N + n0 + col] = s;
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace gf

@@ -1,0 +1,18 @@
+// Instances: EPILOG_NONE and BIAS.
+#include "dispatch.cuh"
+
+namespace gf {
+
+cudaError_t launch_none_bias(int epi, const LaunchArgs& a) {
+  return epi == EPI_BIAS ? launch_epi<EPI_BIAS>(a) : launch_epi<EPI_NONE>(a);
+}
+
+int smem_bytes_for(int tile_n) {
+  return tile_n == 256 ? TileCfg<256>::kSmemBytes : TileCfg<128>::kSmemBytes;
+}
+
+int stages_for(int tile_n) {
+  return tile_n == 256 ? TileCfg<256>::kStages : TileCfg<128>::kStages;
+}
+
+}  // namespace gf

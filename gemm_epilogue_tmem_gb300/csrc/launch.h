@@ -1,0 +1,31 @@
+// Host-side view of the kernels: one launcher per epilog family, each
+// dispatching on dtype, B storage and tile width to a template instance.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "params.h"
+
+namespace gf {
+
+struct LaunchArgs {
+  const CUtensorMap* tmA;
+  const CUtensorMap* tmB;
+  const GemmParams* params;
+  int grid;
+  int bf16;     // 0: fp16, 1: bf16
+  int b_mn;     // 1: B stored [K, N] (MN-major), 0: [N, K] (K-major)
+  int tile_n;   // 128 or 256
+  cudaStream_t stream;
+};
+
+cudaError_t launch_none_bias(int epi, const LaunchArgs& a);   // EPI_NONE, EPI_BIAS
+cudaError_t launch_relu(int epi, const LaunchArgs& a);        // EPI_RELU_BIAS, EPI_RELU_AUX_BIAS
+cudaError_t launch_drelu(const LaunchArgs& a);                // EPI_DRELU_BGRAD
+cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
+                                  cudaStream_t stream);
+int smem_bytes_for(int tile_n);
+int stages_for(int tile_n);
+
+}  // namespace gf

@@ -1,0 +1,40 @@
+// Kernel parameter block and codes shared by the kernels and the host runtime.
+#pragma once
+
+#include <stdint.h>
+
+namespace gf {
+
+enum Epi : int {
+  EPI_NONE = 0,
+  EPI_RELU_BIAS = 1,
+  EPI_RELU_AUX_BIAS = 2,
+  EPI_DRELU_BGRAD = 3,
+  EPI_BIAS = 4,
+};
+
+// bits of the device status word
+enum : int {
+  ST_TIMEOUT_PRODUCER = 1,
+  ST_TIMEOUT_MMA_SMEM = 2,
+  ST_TIMEOUT_MMA_TMEM = 4,
+  ST_TIMEOUT_EPILOGUE = 8,
+  ST_TIMEOUT_DRAIN = 16,
+};
+
+struct GemmParams {
+  int32_t M, N, K;
+  int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+  int32_t bias_axis;     // 0: bias[N] per column, 1: bias[M] per row
+  int32_t bgrad_atomic;  // DRELU_BGRAD: 1 = atomicAdd into bgrad[N], 0 = partials
+  const void* bias;
+  void* out;
+  uint32_t* aux_out;
+  const uint32_t* aux_in;
+  float* bgrad;  // atomic: bgrad[N] (zeroed first); two-pass: partials [num_m_blocks][N]
+  int32_t* status;
+  uint64_t wait_limit_ns;
+  int32_t drop_load;  // test hook: 1-based index of a stage load to skip (0: none)
+};
+
+}  // namespace gf

@@ -1,0 +1,425 @@
+// Host runtime behind include/gf.h: plan validation and tile choice, device
+// workspace, TMA tensor maps and kernel launch.
+//
+// The plan / execute / free split follows the stateful Matmul of the pages
+// ("Fusing Matmul Epilogs with nvmath-python", "Forward-pass capabilities in
+// the source"; nvmath-python / cuBLASLt page, steps 2-3 and "plan reuse"):
+// everything that can be decided once (checks, tile shape, workspace) is done
+// by the plan, and execute only encodes the tensor maps of the caller's
+// pointers and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "gf.h"
+#include "launch.h"
+#include "params.h"
+
+struct gf_plan {
+  int64_t m, n, k;
+  gf_dtype dtype;
+  gf_epilog epilog;
+  gf_bias_axis bias_axis;
+  gf_b_layout b_layout;
+  int device;
+  int num_sms;
+  int tile_n;
+  int forced_tile_n;
+  int stages;
+  int grid;
+  int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+  gf_bgrad_mode bgrad_mode;
+  uint64_t wait_limit_ns;
+  int drop_load;
+  int32_t* d_status;     // device status word (bounded-wait time-outs)
+  float* d_partials;     // [num_m_blocks][n] fp32, DRELU_BGRAD two-pass only
+  size_t partial_bytes;
+};
+
+namespace {
+
+thread_local gf_status g_last = GF_OK;
+
+gf_status fail(gf_status s) {
+  g_last = s;
+  return s;
+}
+
+constexpr int kBM = 128;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetDevice_v2000 g_ctx_get_device = nullptr;
+std::once_flag g_driver_once;
+
+void load_driver_entry_points() {
+  std::call_once(g_driver_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetDevice", &fn, 2000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_device = reinterpret_cast<PFN_cuCtxGetDevice_v2000>(fn);
+  });
+}
+
+// The device of the calling thread's current driver context (the one a
+// framework such as PyTorch made current), else this runtime's device.
+gf_status current_device(int* dev) {
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+    cudaGetLastError();
+    return GF_ERR_NO_DEVICE;
+  }
+  load_driver_entry_points();
+  CUdevice d;
+  if (g_ctx_get_device && g_ctx_get_device(&d) == CUDA_SUCCESS) {
+    *dev = static_cast<int>(d);
+    return GF_OK;
+  }
+  if (cudaGetDevice(dev) != cudaSuccess) return GF_ERR_CUDA;
+  return GF_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool needs_bias(gf_epilog e) {
+  return e == GF_EPILOG_RELU_BIAS || e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_BIAS;
+}
+
+// 2-D tensor map over a row-major [outer, inner] matrix of 16-bit elements,
+// boxes of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt == GF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+void plan_tiles(gf_plan* p) {
+  const int64_t mblocks = (p->m + kBM - 1) / kBM;
+  int tn = p->forced_tile_n;
+  if (tn == 0) {
+    // 256-wide tiles halve the operand traffic per flop; take 128 when the
+    // wide tiles would leave SMs idle
+    const int64_t wide = mblocks * ((p->n + 255) / 256);
+    tn = wide >= p->num_sms ? 256 : 128;
+  }
+  p->tile_n = tn;
+  p->stages = gf::stages_for(tn);
+  p->num_m_blocks = static_cast<int>(mblocks);
+  p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
+  p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
+  const int64_t tiles = mblocks * p->num_n_blocks;
+  p->num_tiles = static_cast<int>(tiles);
+  p->group_m = 8;
+  p->grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
+}
+
+}  // namespace
+
+extern "C" {
+
+GF_API const char* gf_status_string(gf_status s) {
+  switch (s) {
+    case GF_OK: return "GF_OK";
+    case GF_ERR_INVALID_VALUE: return "GF_ERR_INVALID_VALUE: invalid argument";
+    case GF_ERR_UNSUPPORTED: return "GF_ERR_UNSUPPORTED: valid but not supported";
+    case GF_ERR_NO_DEVICE: return "GF_ERR_NO_DEVICE: no CUDA device";
+    case GF_ERR_CUDA: return "GF_ERR_CUDA: a CUDA call failed";
+    case GF_ERR_OUT_OF_MEMORY: return "GF_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    case GF_ERR_DEVICE_TIMEOUT: return "GF_ERR_DEVICE_TIMEOUT: a bounded wait in a kernel gave up";
+  }
+  return "unknown gf_status";
+}
+
+GF_API gf_status gf_last_error(void) { return g_last; }
+
+GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtype,
+                                  gf_epilog epilog, gf_bias_axis bias_axis,
+                                  gf_b_layout b_layout) {
+  g_last = GF_OK;
+  // argument checks first: they need no device
+  if (m < 0 || n < 0 || k < 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  if (dtype != GF_F16 && dtype != GF_BF16) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  if (epilog < GF_EPILOG_NONE || epilog > GF_EPILOG_BIAS) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  if (bias_axis != GF_BIAS_COL && bias_axis != GF_BIAS_ROW) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  if (b_layout != GF_B_KN && b_layout != GF_B_NK) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  if (n % 8 != 0 || k % 8 != 0) {  // 16-byte row strides for the tensor maps
+    fail(GF_ERR_UNSUPPORTED);
+    return nullptr;
+  }
+  if (epilog == GF_EPILOG_DRELU_BGRAD && bias_axis != GF_BIAS_COL) {
+    fail(GF_ERR_UNSUPPORTED);
+    return nullptr;
+  }
+  // ceil(m/128) * ceil(n/128) tiles must fit the int32 tile counter
+  if (((m + 127) / 128) * ((n + 127) / 128) > kMaxDim) {
+    fail(GF_ERR_UNSUPPORTED);
+    return nullptr;
+  }
+
+  int dev = 0;
+  gf_status st = current_device(&dev);
+  if (st != GF_OK) {
+    fail(st);
+    return nullptr;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    fail(GF_ERR_CUDA);
+    return nullptr;
+  }
+  if (prop.major != 10 || prop.minor != 3) {  // the kernels are built for sm_103a only
+    fail(GF_ERR_UNSUPPORTED);
+    return nullptr;
+  }
+  load_driver_entry_points();
+  if (!g_encode) {
+    fail(GF_ERR_CUDA);
+    return nullptr;
+  }
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    fail(GF_ERR_CUDA);
+    return nullptr;
+  }
+
+  gf_plan* p = static_cast<gf_plan*>(calloc(1, sizeof(gf_plan)));
+  if (!p) {
+    fail(GF_ERR_OUT_OF_MEMORY);
+    return nullptr;
+  }
+  p->m = m;
+  p->n = n;
+  p->k = k;
+  p->dtype = dtype;
+  p->epilog = epilog;
+  p->bias_axis = bias_axis;
+  p->b_layout = b_layout;
+  p->device = dev;
+  p->num_sms = prop.multiProcessorCount;
+  p->bgrad_mode = GF_BGRAD_TWO_PASS;
+  p->wait_limit_ns = 2000000000ull;
+  const char* env_tile = getenv("GF_TILE_N");
+  p->forced_tile_n = env_tile && (atoi(env_tile) == 128 || atoi(env_tile) == 256) ? atoi(env_tile) : 0;
+  plan_tiles(p);
+
+  if (cudaMalloc(&p->d_status, 256) != cudaSuccess) {
+    cudaGetLastError();
+    free(p);
+    fail(GF_ERR_OUT_OF_MEMORY);
+    return nullptr;
+  }
+  if (cudaMemset(p->d_status, 0, 256) != cudaSuccess) {
+    cudaFree(p->d_status);
+    free(p);
+    fail(GF_ERR_CUDA);
+    return nullptr;
+  }
+  if (epilog == GF_EPILOG_DRELU_BGRAD && m > 0 && n > 0) {
+    // sized for the narrowest tile so a later tile option never outgrows it
+    p->partial_bytes = static_cast<size_t>((m + kBM - 1) / kBM) * static_cast<size_t>(n) * 4;
+    if (cudaMalloc(&p->d_partials, p->partial_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(p->d_status);
+      free(p);
+      fail(GF_ERR_OUT_OF_MEMORY);
+      return nullptr;
+    }
+  }
+  return p;
+}
+
+GF_API gf_plan* gf_matmul_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, gf_epilog epilog,
+                               gf_bias_axis bias_axis) {
+  return gf_matmul_plan_ex(m, n, k, dtype, epilog, bias_axis, GF_B_KN);
+}
+
+GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value) {
+  if (!p) return fail(GF_ERR_INVALID_VALUE);
+  switch (option) {
+    case GF_OPT_BGRAD_MODE:
+      if (value != GF_BGRAD_TWO_PASS && value != GF_BGRAD_ATOMIC) return fail(GF_ERR_INVALID_VALUE);
+      p->bgrad_mode = static_cast<gf_bgrad_mode>(value);
+      return GF_OK;
+    case GF_OPT_WAIT_LIMIT_US:
+      if (value < 1000 || value > 600000000) return fail(GF_ERR_INVALID_VALUE);
+      p->wait_limit_ns = static_cast<uint64_t>(value) * 1000ull;
+      return GF_OK;
+    case GF_OPT_TILE_N:
+      if (value != 0 && value != 128 && value != 256) return fail(GF_ERR_INVALID_VALUE);
+      p->forced_tile_n = static_cast<int>(value);
+      plan_tiles(p);
+      return GF_OK;
+    case GF_OPT_FAULT_DROP_LOAD:
+      if (value < 0 || value > kMaxDim) return fail(GF_ERR_INVALID_VALUE);
+      p->drop_load = static_cast<int>(value);
+      return GF_OK;
+  }
+  return fail(GF_ERR_INVALID_VALUE);
+}
+
+GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* tile_n,
+                                  int32_t* stages, int32_t* grid, int64_t* workspace_bytes) {
+  if (!p) return fail(GF_ERR_INVALID_VALUE);
+  if (tile_m) *tile_m = kBM;
+  if (tile_n) *tile_n = p->tile_n;
+  if (stages) *stages = p->stages;
+  if (grid) *grid = p->grid;
+  if (workspace_bytes) *workspace_bytes = static_cast<int64_t>(p->partial_bytes) + 256;
+  return GF_OK;
+}
+
+GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* B,
+                                   const void* bias, void* out, const void* aux_in,
+                                   void* aux_out, float* bgrad, struct CUstream_st* stream) {
+  if (!p) return fail(GF_ERR_INVALID_VALUE);
+  const bool empty = p->m == 0 || p->n == 0;
+  const gf_epilog e = p->epilog;
+  // pointer checks: required pointers present and 16-byte aligned
+  if (!empty) {
+    if (!out || !aligned16(out)) return fail(GF_ERR_INVALID_VALUE);
+    if (p->k > 0 && (!A || !B || !aligned16(A) || !aligned16(B)))
+      return fail(GF_ERR_INVALID_VALUE);
+    if (needs_bias(e) && (!bias || !aligned16(bias))) return fail(GF_ERR_INVALID_VALUE);
+    if (e == GF_EPILOG_RELU_AUX_BIAS && (!aux_out || !aligned16(aux_out)))
+      return fail(GF_ERR_INVALID_VALUE);
+    if (e == GF_EPILOG_DRELU_BGRAD && (!aux_in || !aligned16(aux_in)))
+      return fail(GF_ERR_INVALID_VALUE);
+  }
+  if (e == GF_EPILOG_DRELU_BGRAD && p->n > 0 && (!bgrad || !aligned16(bgrad)))
+    return fail(GF_ERR_INVALID_VALUE);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaSetDevice(p->device) != cudaSuccess) return fail(GF_ERR_CUDA);
+
+  if (empty) {
+    // nothing to multiply; the bias gradient of zero rows is zero
+    if (e == GF_EPILOG_DRELU_BGRAD && p->n > 0 &&
+        cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
+    return GF_OK;
+  }
+
+  CUtensorMap tmA, tmB;
+  memset(&tmA, 0, sizeof tmA);
+  memset(&tmB, 0, sizeof tmB);
+  if (p->k > 0) {
+    if (!encode_2d(&tmA, A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
+    const bool ok = p->b_layout == GF_B_KN
+                        ? encode_2d(&tmB, B, p->dtype, p->n, p->k, 64, 64)
+                        : encode_2d(&tmB, B, p->dtype, p->k, p->n, 64, p->tile_n);
+    if (!ok) return fail(GF_ERR_INVALID_VALUE);
+  }
+
+  gf::GemmParams prm;
+  memset(&prm, 0, sizeof prm);
+  prm.M = static_cast<int32_t>(p->m);
+  prm.N = static_cast<int32_t>(p->n);
+  prm.K = static_cast<int32_t>(p->k);
+  prm.num_m_blocks = p->num_m_blocks;
+  prm.num_n_blocks = p->num_n_blocks;
+  prm.num_k_blocks = p->num_k_blocks;
+  prm.num_tiles = p->num_tiles;
+  prm.group_m = p->group_m;
+  prm.bias_axis = p->bias_axis == GF_BIAS_ROW ? 1 : 0;
+  prm.bias = bias;
+  prm.out = out;
+  prm.aux_out = static_cast<uint32_t*>(aux_out);
+  prm.aux_in = static_cast<const uint32_t*>(aux_in);
+  prm.status = p->d_status;
+  prm.wait_limit_ns = p->wait_limit_ns;
+  prm.drop_load = p->drop_load;
+
+  const bool atomic = e == GF_EPILOG_DRELU_BGRAD && p->bgrad_mode == GF_BGRAD_ATOMIC;
+  if (e == GF_EPILOG_DRELU_BGRAD) {
+    prm.bgrad_atomic = atomic ? 1 : 0;
+    prm.bgrad = atomic ? bgrad : p->d_partials;
+    if (atomic && cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
+  }
+
+  gf::LaunchArgs la;
+  la.tmA = &tmA;
+  la.tmB = &tmB;
+  la.params = &prm;
+  la.grid = p->grid;
+  la.bf16 = p->dtype == GF_BF16 ? 1 : 0;
+  la.b_mn = p->b_layout == GF_B_KN ? 1 : 0;
+  la.tile_n = p->tile_n;
+  la.stream = st;
+
+  cudaError_t err;
+  switch (e) {
+    case GF_EPILOG_NONE: err = gf::launch_none_bias(gf::EPI_NONE, la); break;
+    case GF_EPILOG_BIAS: err = gf::launch_none_bias(gf::EPI_BIAS, la); break;
+    case GF_EPILOG_RELU_BIAS: err = gf::launch_relu(gf::EPI_RELU_BIAS, la); break;
+    case GF_EPILOG_RELU_AUX_BIAS: err = gf::launch_relu(gf::EPI_RELU_AUX_BIAS, la); break;
+    case GF_EPILOG_DRELU_BGRAD: err = gf::launch_drelu(la); break;
+    default: return fail(GF_ERR_INVALID_VALUE);
+  }
+  if (err != cudaSuccess) return fail(GF_ERR_CUDA);
+  if (e == GF_EPILOG_DRELU_BGRAD && !atomic) {
+    err = gf::launch_bgrad_finalize(p->d_partials, p->num_m_blocks, static_cast<int>(p->n), bgrad,
+                                    st);
+    if (err != cudaSuccess) return fail(GF_ERR_CUDA);
+  }
+  return GF_OK;
+}
+
+GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {
+  if (!p) return fail(GF_ERR_INVALID_VALUE);
+  if (cudaSetDevice(p->device) != cudaSuccess) return fail(GF_ERR_CUDA);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return fail(GF_ERR_CUDA);
+  int32_t word = 0;
+  if (cudaMemcpy(&word, p->d_status, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(GF_ERR_CUDA);
+  if (word != 0) {
+    if (cudaMemset(p->d_status, 0, 4) != cudaSuccess) return fail(GF_ERR_CUDA);
+    return fail(GF_ERR_DEVICE_TIMEOUT);
+  }
+  return GF_OK;
+}
+
+GF_API void gf_plan_free(gf_plan* p) {
+  if (!p) return;
+  cudaSetDevice(p->device);
+  if (p->d_partials) cudaFree(p->d_partials);
+  if (p->d_status) cudaFree(p->d_status);
+  free(p);
+}
+
+}  // extern "C"

@@ -1,0 +1,207 @@
+/*
+ * gf -- fused GEMM + epilogue on GB300 (sm_103a): the C ABI.
+ *
+ * One dense half-precision matrix multiply per call, with the epilogue run
+ * inside the same kernel while the fp32 accumulator is still on chip:
+ *
+ *   out[M,N] = epilog( A[M,K] . B[K,N] )      fp16/bf16 in, fp32 accumulate
+ *
+ * The operations follow these web pages on fused matmul epilogs:
+ *  - "Fusing Matmul Epilogs with nvmath-python": "The problem addressed by
+ *    fused epilogs" (product + bias per output column + ReLU in one call),
+ *    "Forward-pass capabilities in the source" (RELU_BIAS, RELU_AUX_BIAS and
+ *    its bit-encoded relu_aux mask; the stateful plan / execute split),
+ *    "Backward-pass path shown in the example" (DRELU_BGRAD: the product with
+ *    the transposed weight, masked by relu_aux, plus the column-wise sum that
+ *    is the bias gradient).
+ *  - "nvmath-python 封装 cuBLASLt ..." (nvmath-python over cuBLASLt): step 1
+ *    (fp16 operands, bias of shape (m,1)), step 2 (plan with
+ *    COMPUTE_32F_FAST_16F: fp32 accumulation; epilog and epilog inputs fixed
+ *    at plan time), step 3 (execute is asynchronous on a stream; free
+ *    releases the plan), "plan reuse" (planning is the expensive step,
+ *    execute is light and reused for equal shape, dtype and epilog), "other
+ *    epilogs" (BIAS, GELU_BIAS).
+ *
+ * Conventions for every call:
+ *  - Matrices are dense and row-major. A is [m, k]. B is [k, n]
+ *    (GF_B_KN, the default) or given as an [n, k] matrix W with B = W^T
+ *    (GF_B_NK: an nn.Linear weight, or the transposed weight of a backward
+ *    pass). out is [m, n].
+ *  - Device pointers are caller-owned device memory (for example torch
+ *    tensors), 16-byte aligned. The library never frees them.
+ *  - relu_aux words: uint32 [ceil(m/32), n] row-major. Bit (i % 32) of word
+ *    [i/32][j] is 1 when the fp32 pre-activation z[i][j] = acc + bias is
+ *    strictly greater than 0. Bits of rows >= m are 0.
+ *  - Errors: a call that fails returns a gf_status (or NULL for the plan
+ *    constructors) and records it for gf_last_error() on the calling thread.
+ *    Invalid arguments are rejected before anything is enqueued.
+ *  - The stream argument is a cudaStream_t (NULL: the legacy default stream),
+ *    declared through its underlying struct so this header needs no CUDA
+ *    header.
+ */
+#ifndef GF_H
+#define GF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GF_API __attribute__((visibility("default")))
+#else
+#define GF_API
+#endif
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
+
+typedef enum gf_status {
+  GF_OK = 0,
+  GF_ERR_INVALID_VALUE = 1,   /* bad argument: NULL, size, alignment, enum  */
+  GF_ERR_UNSUPPORTED = 2,     /* valid but not handled (shape rule, device) */
+  GF_ERR_NO_DEVICE = 3,       /* no CUDA device could be queried            */
+  GF_ERR_CUDA = 4,            /* a CUDA runtime or driver call failed       */
+  GF_ERR_OUT_OF_MEMORY = 5,   /* plan workspace could not be allocated      */
+  GF_ERR_DEVICE_TIMEOUT = 6   /* a bounded wait inside a kernel gave up     */
+} gf_status;
+
+typedef enum gf_dtype {
+  GF_F16 = 0, /* IEEE binary16 in and out */
+  GF_BF16 = 1 /* bfloat16 in and out      */
+} gf_dtype;
+
+typedef enum gf_epilog {
+  GF_EPILOG_NONE = 0,          /* out = acc                                      */
+  GF_EPILOG_RELU_BIAS = 1,     /* out = max(acc + bias, 0)                       */
+  GF_EPILOG_RELU_AUX_BIAS = 2, /* RELU_BIAS, and aux_out = relu_aux words        */
+  GF_EPILOG_DRELU_BGRAD = 3,   /* out = acc masked by aux_in; bgrad = colsum(out) */
+  GF_EPILOG_BIAS = 4           /* out = acc + bias                               */
+} gf_epilog;
+
+typedef enum gf_bias_axis {
+  GF_BIAS_COL = 0, /* bias[n]: one value per output column, broadcast down rows */
+  GF_BIAS_ROW = 1  /* bias[m]: one value per output row (a (m,1) bias)          */
+} gf_bias_axis;
+
+typedef enum gf_b_layout {
+  GF_B_KN = 0, /* B stored [k, n] row-major                        */
+  GF_B_NK = 1  /* B = W^T with W stored [n, k] row-major          */
+} gf_b_layout;
+
+typedef enum gf_bgrad_mode {
+  GF_BGRAD_TWO_PASS = 0, /* per-tile fp32 partial sums, then a fixed-order sum: deterministic */
+  GF_BGRAD_ATOMIC = 1    /* one fp32 atomicAdd per column per tile: run-to-run order varies  */
+} gf_bgrad_mode;
+
+typedef struct gf_plan gf_plan;
+
+/*
+ * Plan one fused GEMM + epilogue: validates the problem, checks that the
+ * current CUDA device is an sm_103 GPU, picks the tile configuration and
+ * allocates the plan's device workspace (status word; bgrad partial sums for
+ * DRELU_BGRAD). Host only; enqueues nothing. Equivalent to
+ * gf_matmul_plan_ex(..., GF_B_KN).
+ *
+ * Source: the plan step of the stateful Matmul ("Fusing Matmul Epilogs with
+ * nvmath-python", "Forward-pass capabilities in the source"; nvmath-python /
+ * cuBLASLt page, step 2 and "plan reuse").
+ *
+ * m, n, k   : problem size, 0 <= m, n, k < 2^31; n % 8 == 0 and k % 8 == 0
+ *             (16-byte row strides), else GF_ERR_UNSUPPORTED. m, n or k may be
+ *             0 (an empty product; k == 0 makes acc = 0).
+ * dtype     : element type of A, B, bias and out.
+ * epilog    : one of gf_epilog.
+ * bias_axis : GF_BIAS_COL or GF_BIAS_ROW; DRELU_BGRAD needs GF_BIAS_COL (its
+ *             bias gradient is per column), else GF_ERR_UNSUPPORTED. Ignored by
+ *             GF_EPILOG_NONE.
+ * Returns a library-owned plan (release with gf_plan_free), or NULL with the
+ * reason in gf_last_error().
+ */
+GF_API gf_plan* gf_matmul_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, gf_epilog epilog,
+                               gf_bias_axis bias_axis);
+
+/* gf_matmul_plan with the storage of B given explicitly (see gf_b_layout).
+ * The backward of a linear layer multiplies by W^T for the forward weight W
+ * ("Backward-pass path shown in the example"): that is GF_B_NK with W. */
+GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtype,
+                                  gf_epilog epilog, gf_bias_axis bias_axis,
+                                  gf_b_layout b_layout);
+
+/*
+ * Enqueue the planned GEMM + epilogue on `stream` and return at once (the
+ * nvmath-python / cuBLASLt page, step 3: execution does not block; the
+ * caller synchronises). One kernel launch, plus one small finalize launch
+ * for DRELU_BGRAD in GF_BGRAD_TWO_PASS mode.
+ *
+ * A       : device [m, k].
+ * B       : device [k, n] (GF_B_KN) or [n, k] (GF_B_NK).
+ * bias    : device, n (GF_BIAS_COL) or m (GF_BIAS_ROW) elements of dtype.
+ *           Required by RELU_BIAS, RELU_AUX_BIAS and BIAS; ignored otherwise.
+ * out     : device [m, n] of dtype. Always required (when m*n > 0).
+ * aux_in  : device relu_aux words [ceil(m/32), n] from a RELU_AUX_BIAS
+ *           forward. Required by DRELU_BGRAD; ignored otherwise.
+ * aux_out : device relu_aux words [ceil(m/32), n], written in full.
+ *           Required by RELU_AUX_BIAS; ignored otherwise.
+ * bgrad   : device fp32 [n], overwritten with the column sums of the masked
+ *           fp32 product. Required by DRELU_BGRAD; ignored otherwise.
+ * A missing required pointer or a pointer not 16-byte aligned gives
+ * GF_ERR_INVALID_VALUE; a failed launch gives GF_ERR_CUDA. The plan's
+ * workspace is shared by its calls: use one plan from one stream at a time.
+ */
+GF_API gf_status gf_matmul_execute(const gf_plan* plan, const void* A, const void* B,
+                                   const void* bias, void* out, const void* aux_in,
+                                   void* aux_out, float* bgrad, struct CUstream_st* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the plan's device status word.
+ * Returns GF_ERR_DEVICE_TIMEOUT if a bounded wait in a kernel of this plan
+ * gave up since the last call (the kernel then skipped the rest of its work
+ * and returned; its outputs are incomplete), GF_ERR_CUDA if the stream
+ * reports an error, else GF_OK. Not on the pages: the library's failure
+ * detection.
+ */
+GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream);
+
+/*
+ * Plan options (not on the pages; tuning and failure-detection knobs).
+ * GF_OPT_BGRAD_MODE      : a gf_bgrad_mode (default GF_BGRAD_TWO_PASS).
+ * GF_OPT_WAIT_LIMIT_US   : the limit of every bounded wait inside the kernel,
+ *                          in microseconds (default 2000000, min 1000).
+ * GF_OPT_TILE_N          : output tile width, 128 or 256 (0: the plan's choice).
+ * GF_OPT_FAULT_DROP_LOAD : test hook. When v > 0 the producer skips its v-th
+ *                          stage load, so the consumer's bounded wait runs
+ *                          out; execute then completes with
+ *                          GF_ERR_DEVICE_TIMEOUT from gf_plan_status. 0: off.
+ * Returns GF_ERR_INVALID_VALUE for an unknown option or value.
+ */
+typedef enum gf_option {
+  GF_OPT_BGRAD_MODE = 0,
+  GF_OPT_WAIT_LIMIT_US = 1,
+  GF_OPT_TILE_N = 2,
+  GF_OPT_FAULT_DROP_LOAD = 3
+} gf_option;
+
+GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);
+
+/* Read back the plan's choices: tile_m, tile_n, stages, grid size (CTAs per
+ * launch), workspace bytes. Any out-pointer may be NULL. */
+GF_API gf_status gf_plan_describe(const gf_plan* plan, int32_t* tile_m, int32_t* tile_n,
+                                  int32_t* stages, int32_t* grid, int64_t* workspace_bytes);
+
+/* Release the plan and its workspace ("free" on the nvmath-python / cuBLASLt
+ * page, step 3). Caller tensors are untouched. NULL is a no-op. Work already
+ * enqueued with the plan must have completed. */
+GF_API void gf_plan_free(gf_plan* plan);
+
+/* Static text for a status code. */
+GF_API const char* gf_status_string(gf_status status);
+
+/* The status of the last failing call on this thread (GF_OK if none). */
+GF_API gf_status gf_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GF_H */
