@@ -50,8 +50,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete, giving up after
-// `limit_ns` of global time or as soon as *abort is set. Returns false when
-// it gave up. Every wait in the kernels goes through here.
+// `limit_ns` of global time or as soon as *abort is set (abort may be null:
+// the wait then ends on time alone). Returns false when it gave up. Every
+// wait in the kernels goes through here.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -59,7 +60,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
