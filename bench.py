@@ -371,8 +371,54 @@ def run_gpu(args):
     return 0
 
 
+def run_profile_case(args):
+    """One fused GEMM + epilogue of the given shape, launched warmup + steps
+    times: the small case the ncu captures run (no oracle, no timing)."""
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+
+    m, n, k = (int(x) for x in args.profile_case.split(","))
+    epi = {"relu_aux_bias": gf.GF_EPILOG_RELU_AUX_BIAS, "drelu_bgrad": gf.GF_EPILOG_DRELU_BGRAD,
+           "none": gf.GF_EPILOG_NONE, "relu_bias": gf.GF_EPILOG_RELU_BIAS}[args.epilog]
+    layout = gf.GF_B_NK if epi == gf.GF_EPILOG_DRELU_BGRAD else gf.GF_B_KN
+    gf.build()
+    synth.build_cuda()
+    dev = torch.device("cuda", 0)
+    sp = torch.cuda.current_stream().cuda_stream
+    A = torch.empty((m, k), dtype=torch.float16, device=dev)
+    B = torch.empty((k, n) if layout == gf.GF_B_KN else (n, k), dtype=torch.float16, device=dev)
+    bias = torch.empty((n,), dtype=torch.float16, device=dev)
+    out = torch.empty((m, n), dtype=torch.float16, device=dev)
+    aux = torch.empty(((m + 31) // 32, n), dtype=torch.int32, device=dev)
+    bgrad = torch.empty((n,), dtype=torch.float32, device=dev)
+    synth.dev_normal(A, synth.F16, 0, synth.TID_A, 1.0, sp)
+    synth.dev_normal(B, synth.F16, 0, synth.TID_B, 1 / np.sqrt(k), sp)
+    synth.dev_normal(bias, synth.F16, 0, synth.TID_BIAS, 0.1, sp)
+    synth.dev_mask_words(aux, m, n, 0, synth.TID_MASK, sp)
+    plan = gf.gf_matmul_plan_ex(m, n, k, gf.GF_F16, epi, gf.GF_BIAS_COL, layout)
+    if args.kernel:
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, args.kernel)
+    for _ in range(args.warmup + args.steps):
+        if epi == gf.GF_EPILOG_DRELU_BGRAD:
+            gf.gf_matmul_execute(plan, A, B, out=out, aux_in=aux, bgrad=bgrad, stream=sp)
+        else:
+            gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=aux, stream=sp)
+    torch.cuda.synchronize()
+    st = gf.gf_plan_status(plan, sp)
+    print(json.dumps({"profile_case": [m, n, k], "epilog": args.epilog, "status": st,
+                      "plan": gf.gf_plan_describe(plan)}))
+    plan.free()
+    return 0 if st == gf.GF_OK else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", default="",
+                    help="M,N,K: run one fused GEMM of this shape (for ncu captures)")
+    ap.add_argument("--epilog", default="relu_aux_bias",
+                    choices=["relu_aux_bias", "drelu_bgrad", "none", "relu_bias"])
+    ap.add_argument("--kernel", type=int, default=0, help="0 plan's choice, 1 single CTA, 2 pair")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
@@ -386,6 +432,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_case:
+        return run_profile_case(args)
     return run_gpu(args)
 
 

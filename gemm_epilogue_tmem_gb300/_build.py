@@ -18,7 +18,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgf.so")
 
 SOURCES = ["runtime.cu", "k_none_bias.cu", "k_relu.cu", "k_drelu.cu"]
-HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "dispatch.cuh", "launch.h", "params.h"]
+HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "gemm_kernel_2sm.cuh", "dispatch.cuh", "launch.h",
+           "params.h"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",

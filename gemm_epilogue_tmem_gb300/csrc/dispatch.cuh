@@ -2,6 +2,7 @@
 #pragma once
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_2sm.cuh"
 #include "launch.h"
 
 namespace gf {
@@ -21,8 +22,65 @@ cudaError_t launch_instance(const LaunchArgs& a) {
   return cudaGetLastError();
 }
 
+template <int EPI, typename T, bool B_MN>
+cudaError_t launch_pair_instance(const LaunchArgs& a) {
+  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
+  constexpr int smem = PairCfg::kSmemBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.params);
+}
+
+// Largest number of CTA pairs of this instance that can be resident at once.
+template <int EPI, typename T, bool B_MN>
+int pair_max_clusters() {
+  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
+  constexpr int smem = PairCfg::kSmemBytes;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
 template <int EPI>
 cudaError_t launch_epi(const LaunchArgs& a) {
+  if (a.pair) {
+    if (a.bf16)
+      return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true>(a)
+                    : launch_pair_instance<EPI, __nv_bfloat16, false>(a);
+    return a.b_mn ? launch_pair_instance<EPI, __half, true>(a)
+                  : launch_pair_instance<EPI, __half, false>(a);
+  }
   if (a.tile_n == 256) {
     if (a.bf16)
       return a.b_mn ? launch_instance<EPI, __nv_bfloat16, true, 256>(a)

@@ -107,6 +107,136 @@ __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* a
   atomicOr(p.status, code);
 }
 
+// Drain one 128-row x BN accumulator from tensor memory and apply the
+// epilog. Warp quarter q owns TMEM lanes 32q..32q+31 = output rows
+// row0 + 32q + lane; t_row addresses (lane 32q, first column of the buffer).
+template <int EPI, typename T, int BN>
+__device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
+                                               int n0, int q, uint32_t lane, float* red) {
+  const int row = row0 + 32 * q + (int)lane;
+  const bool row_ok = row < p.M;
+  const int wrow = (row0 >> 5) + q;  // relu_aux word row of this warp's 32 rows
+  const bool wrow_ok = row0 + 32 * q < p.M;
+  const T* bias = reinterpret_cast<const T*>(p.bias);
+  float row_bias = 0.f;
+  if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS || EPI == EPI_BIAS) {
+    if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
+  }
+  T* out = reinterpret_cast<T*>(p.out);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int col0 = n0 + 32 * c;
+    if (col0 >= p.N) break;  // same for every epilogue warp
+    float v[32];
+    if (p.num_k_blocks > 0) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + 32u * c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    }
+
+    if constexpr (EPI == EPI_DRELU_BGRAD) {
+      uint32_t my_word = 0;
+      if (wrow_ok && col0 + (int)lane < p.N)
+        my_word = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t w = __shfl_sync(0xFFFFFFFFu, my_word, j);
+        v[j] = ((w >> lane) & 1u) ? v[j] : 0.f;
+      }
+    } else if constexpr (EPI != EPI_NONE) {
+      if (p.bias_axis == 0) {
+        const T* bp = bias + col0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float b8[8];
+          if (col0 + 8 * g < p.N) {
+            unpack8<T>(__ldg(reinterpret_cast<const uint4*>(bp + 8 * g)), b8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) b8[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] + b8[i];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = v[j] + row_bias;
+      }
+      if constexpr (EPI == EPI_RELU_AUX_BIAS) {
+        uint32_t my_word = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_ok && v[j] > 0.f);
+          my_word = (lane == (uint32_t)j) ? bal : my_word;
+        }
+        if (wrow_ok && col0 + (int)lane < p.N)
+          p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
+      }
+      if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
+      }
+    }
+
+    if (row_ok) {
+      T* op = out + (size_t)row * p.N + col0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        if (col0 + 8 * g < p.N) {
+          uint4 u;
+          u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
+          u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
+          u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
+          u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
+          *reinterpret_cast<uint4*>(op + 8 * g) = u;
+        }
+      }
+    }
+
+    if constexpr (EPI == EPI_DRELU_BGRAD) {
+      // transpose-reduce: after 5 halving steps (31 shuffles) lane l
+      // holds the sum of column col0 + l over this warp's 32 rows
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & (uint32_t)o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+          const float send = upper ? v[i] : v[i + o];
+          const float keep = upper ? v[i + o] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+      }
+      red[q * BN + 32 * c + (int)lane] = v[0];
+    }
+  }
+}
+
+// Column sums of the tile's 128 rows: the four warps' 32-row sums (in red,
+// [4][BN]) added in a fixed order, then one partial per 128-row block or one
+// atomicAdd per column. Called by the 128 epilogue threads (ep_tid 0..127).
+template <int BN>
+__device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float* red, int ep_tid,
+                                               int n0, int mb) {
+  if (mb >= p.num_m_blocks) return;  // rows past M (same for all 128 threads): nothing to add
+  named_bar_sync(1, 128);
+  for (int col = ep_tid; col < BN; col += 128) {
+    if (n0 + col < p.N) {
+      // the four warps' 32-row sums, always in the same order
+      const float s = ((red[col] + red[BN + col]) + red[2 * BN + col]) + red[3 * BN + col];
+      if (p.bgrad_atomic)
+        atomicAdd(p.bgrad + n0 + col, s);
+      else
+        p.bgrad[(size_t)mb * p.N + n0 + col] = s;
+    }
+  }
+  named_bar_sync(1, 128);
+}
+
 template <int EPI, typename T, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilog_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -287,128 +417,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m0 = mb * kBM, n0 = nb * BN;
-      const int row = m0 + 32 * q + (int)lane;
-      const bool row_ok = row < p.M;
-      const int wrow = (m0 >> 5) + q;  // relu_aux word row of this warp's 32 rows
-      const bool wrow_ok = m0 + 32 * q < p.M;
-      const T* bias = reinterpret_cast<const T*>(p.bias);
-      float row_bias = 0.f;
-      if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS || EPI == EPI_BIAS) {
-        if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
-      }
-      T* out = reinterpret_cast<T*>(p.out);
       const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN);
 
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n0 + 32 * c;
-        if (col0 >= p.N) break;  // same for every epilogue warp
-        float v[32];
-        if (p.num_k_blocks > 0) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_row + 32u * c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-
-        if constexpr (EPI == EPI_DRELU_BGRAD) {
-          uint32_t my_word = 0;
-          if (wrow_ok && col0 + (int)lane < p.N)
-            my_word = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t w = __shfl_sync(0xFFFFFFFFu, my_word, j);
-            v[j] = ((w >> lane) & 1u) ? v[j] : 0.f;
-          }
-        } else if constexpr (EPI != EPI_NONE) {
-          if (p.bias_axis == 0) {
-            const T* bp = bias + col0;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              float b8[8];
-              if (col0 + 8 * g < p.N) {
-                unpack8<T>(__ldg(reinterpret_cast<const uint4*>(bp + 8 * g)), b8);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) b8[i] = 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] + b8[i];
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = v[j] + row_bias;
-          }
-          if constexpr (EPI == EPI_RELU_AUX_BIAS) {
-            uint32_t my_word = 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_ok && v[j] > 0.f);
-              my_word = (lane == (uint32_t)j) ? bal : my_word;
-            }
-            if (wrow_ok && col0 + (int)lane < p.N)
-              p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
-          }
-          if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
-          }
-        }
-
-        if (row_ok) {
-          T* op = out + (size_t)row * p.N + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + 8 * g < p.N) {
-              uint4 u;
-              u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
-              u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
-              u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
-              u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
-              *reinterpret_cast<uint4*>(op + 8 * g) = u;
-            }
-          }
-        }
-
-        if constexpr (EPI == EPI_DRELU_BGRAD) {
-          // transpose-reduce: after 5 halving steps (31 shuffles) lane l
-          // holds the sum of column col0 + l over this warp's 32 rows
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
-            const bool upper = (lane & (uint32_t)o) != 0;
-#pragma unroll
-            for (int i = 0; i < o; ++i) {
-              const float send = upper ? v[i] : v[i + o];
-              const float keep = upper ? v[i + o] : v[i];
-              v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-            }
-          }
-          red[q * BN + 32 * c + (int)lane] = v[0];
-        }
-      }
+      epilogue_drain<EPI, T, BN>(p, t_row, m0, n0, q, lane, red);
       // accumulator buffer drained: the MMA warp may reuse it
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8u * buf);
 
-      if constexpr (EPI == EPI_DRELU_BGRAD) {
-        named_bar_sync(1, 128);
-        for (int col = ep_tid; col < BN; col += 128) {
-          if (n0 + col < p.N) {
-            // the four warps' 32-row sums, always in the same order
-            const float s = ((red[col] + red[BN + col]) + red[2 * BN + col]) + red[3 * BN + col];
-            if (p.bgrad_atomic)
-              atomicAdd(p.bgrad + n0 + col, s);
-            else
-              p.bgrad[(size_t)mb * p.N + n0 + col] = s;
-          }
-        }
-        named_bar_sync(1, 128);
-      }
+      if constexpr (EPI == EPI_DRELU_BGRAD) epilogue_bgrad<BN>(p, red, ep_tid, n0, mb);
     }
   }
 

@@ -1,0 +1,256 @@
+// CTA-pair variant of the fused GEMM + epilogue kernel: a cluster of two
+// CTAs on two SMs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction).
+//
+//   - Each CTA loads its own 128 rows of A and its own 128 columns of B for
+//     every k-slice (TMA, 128-byte swizzle, no multicast): per SM the operand
+//     traffic per flop is 2/3 of the single-CTA 128 x 256 tile's.
+//   - The stage-full barrier lives in the leader CTA (rank 0): the leader's
+//     producer expects the bytes of both CTAs, the peer's TMA loads signal
+//     the leader's barrier (.cta_group::2).
+//   - The leader's MMA thread issues the pair MMA; commits are multicast to
+//     both CTAs (stage-empty, accumulator-full barriers).
+//   - Each CTA drains its own 128 TMEM lanes (its 128 rows x 256 columns)
+//     with the same epilogue as the single-CTA kernel; both CTAs' epilogue
+//     warps release the accumulator buffer on the leader's barrier.
+//   - Teardown: drains, then a cluster barrier, then a pair TMEM dealloc.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace gf {
+
+struct PairCfg {
+  static constexpr int BN = 256;          // pair tile 256 x 256, each CTA 128 x 256
+  static constexpr int kStages = 6;
+  static constexpr int kABytes = kBM * kBK * 2;          // 16 KB: this CTA's 128 rows
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;     // 16 KB: this CTA's 128 columns
+  static constexpr int kTmemCols = 2 * BN;               // two accumulator buffers
+  static constexpr int kCtrlBytes = 1024;
+  static constexpr int kRedBytes = 4 * BN * 4;
+  static constexpr int kSmemBytes =
+      1024 + kStages * (kABytes + kBBytes) + kCtrlBytes + kRedBytes;
+};
+
+// Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
+__device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int& mb2, int& nb) {
+  const int num_m2 = (p.num_m_blocks + 1) / 2;
+  const int group_size = p.group_m * p.num_n_blocks;
+  const int group = t / group_size;
+  const int first_m = group * p.group_m;
+  const int gm = min(num_m2 - first_m, p.group_m);
+  const int r = t - group * group_size;
+  mb2 = first_m + r % gm;
+  nb = r / gm;
+}
+
+template <int EPI, typename T, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  using C = PairCfg;
+  constexpr int S = C::kStages;
+  constexpr int BN = C::BN;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  extern __shared__ uint8_t smem_raw[];
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + S * C::kABytes;
+  const uint32_t ctrl = sB + S * C::kBBytes;
+  uint8_t* gctrl = gbase + (ctrl - base);
+  const uint32_t full0 = ctrl;              // leader: S barriers, stage filled (both CTAs' bytes)
+  const uint32_t empty0 = ctrl + 8u * S;    // both: S barriers, stage consumed
+  const uint32_t tfull0 = ctrl + 16u * S;   // both: 2 barriers, accumulator ready
+  const uint32_t tempty0 = tfull0 + 16u;    // leader: 2 barriers, accumulator drained (8 warps)
+  const uint32_t done_bar = tempty0 + 16u;  // leader: MMA teardown
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gctrl + 16 * S + 40);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 44);
+  float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x >> 1;
+  const int num_clusters = gridDim.x >> 1;
+  const int num_pair_tiles = p.num_tiles;  // the host counts pair tiles for this kernel
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, 1);
+    }
+    mbar_init(tfull0, 1);
+    mbar_init(tfull0 + 8u, 1);
+    mbar_init(tempty0, 8);
+    mbar_init(tempty0 + 8u, 8);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (p.num_k_blocks > 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && p.num_k_blocks > 0) {
+      int issued[S];
+#pragma unroll
+      for (int s = 0; s < S; ++s) issued[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int loads = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < num_pair_tiles && ok; t += num_clusters) {
+        int mb2, nb;
+        pair_tile_coords(p, t, mb2, nb);
+        const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
+        const int n_col = nb * BN + 128 * (int)rank;    // this CTA's B columns
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
+            ok = false;
+            aborted = true;
+            break;
+          }
+          ++loads;
+          if (loads != p.drop_load) {
+            const uint32_t fb_local = full0 + 8u * stage;
+            const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
+            if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kBBytes));
+            tma_load_2d_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row);
+            if (B_MN) {
+              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, fb, n_col, kb * kBK);
+              tma_load_2d_pair(sB + stage * C::kBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
+                               kb * kBK);
+            } else {
+              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, fb, kb * kBK, n_col);
+            }
+            issued[stage] = (int)phase;
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the leader's full barriers count both CTAs' bytes: when they have
+      // completed, every load of the pair has landed
+      if (leader) {
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+          if (issued[s] >= 0 &&
+              !mbar_wait_bounded(full0 + 8u * s, (uint32_t)issued[s], nullptr, p.wait_limit_ns))
+            raise_error(p, abort_flag, ST_TIMEOUT_DRAIN);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA (leader)
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_f16(kBf16, B_MN, 256, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = cluster_id; t < num_pair_tiles && ok; t += num_clusters, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_bounded_cluster(tempty0 + 8u * buf, use ^ 1u, abort_flag,
+                                       p.wait_limit_ns)) {
+          raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        if (p.num_k_blocks == 0) {
+          umma_commit_pair(tfull0 + 8u * buf, 0x3);  // nothing to multiply: acc is zero
+          continue;
+        }
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
+            ok = false;
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = sA + stage * C::kABytes;
+          const uint32_t b_base = sB + stage * C::kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
+                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(tfull0 + 8u * buf, 0x3);
+      }
+      umma_commit_pair(done_bar, 0x1);
+      if (!mbar_wait_bounded(done_bar, 0, nullptr, p.wait_limit_ns))
+        raise_error(p, abort_flag, ST_TIMEOUT_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int ep_tid = threadIdx.x - 64;
+    const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+    int it = 0;
+    for (int t = cluster_id; t < num_pair_tiles; t += num_clusters, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
+      if constexpr (EPI == EPI_DRELU_BGRAD) ok = !named_bar_red_or(1, 128, !ok);
+      if (!ok) {
+        raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      int mb2, nb;
+      pair_tile_coords(p, t, mb2, nb);
+      const int row0 = mb2 * 256 + 128 * (int)rank;
+      const int n0 = nb * BN;
+      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN);
+      epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(tempty_leader);
+      if constexpr (EPI == EPI_DRELU_BGRAD) epilogue_bgrad<BN>(p, red, ep_tid, n0, row0 / kBM);
+    }
+  }
+
+  // a CTA that gave up may still have loads in flight towards its shared
+  // memory that no barrier of its own tracks: give them time to land
+  if (__syncthreads_or(aborted ? 1 : 0) || *abort_flag) sleep_ns(200000);
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace gf

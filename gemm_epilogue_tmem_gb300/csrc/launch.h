@@ -16,7 +16,8 @@ struct LaunchArgs {
   int grid;
   int bf16;     // 0: fp16, 1: bf16
   int b_mn;     // 1: B stored [K, N] (MN-major), 0: [N, K] (K-major)
-  int tile_n;   // 128 or 256
+  int tile_n;   // 128 or 256 (single-CTA kernel)
+  int pair;     // 1: the CTA-pair kernel (256 x 256 tiles)
   cudaStream_t stream;
 };
 
@@ -27,5 +28,8 @@ cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n,
                                   cudaStream_t stream);
 int smem_bytes_for(int tile_n);
 int stages_for(int tile_n);
+int pair_stages();
+// resident CTA pairs of the pair kernel (0 if it cannot launch)
+int pair_max_clusters_any();
 
 }  // namespace gf

@@ -30,6 +30,9 @@ struct gf_plan {
   int num_sms;
   int tile_n;
   int forced_tile_n;
+  int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair
+  int pair;              // the plan uses the CTA-pair kernel
+  int max_pair_clusters; // resident CTA pairs (0: the pair kernel cannot run)
   int stages;
   int grid;
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
@@ -115,21 +118,42 @@ bool encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner, u
 
 void plan_tiles(gf_plan* p) {
   const int64_t mblocks = (p->m + kBM - 1) / kBM;
+  p->num_m_blocks = static_cast<int>(mblocks);
+  p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
+  p->group_m = 8;
+  // The CTA-pair kernel (256 x 256 tiles over two SMs) moves 2/3 of the
+  // operand bytes per flop of the single-CTA 128 x 256 tile; take it when its
+  // tiles fill the resident pairs, else the single-CTA kernel with the tile
+  // width that keeps the SMs busy.
+  const int64_t pair_tiles = ((p->m + 255) / 256) * ((p->n + 255) / 256);
+  bool pair = false;
+  if (p->forced_kernel == 2)
+    pair = p->max_pair_clusters > 0;
+  else if (p->forced_kernel == 0)
+    pair = p->max_pair_clusters > 0 && p->forced_tile_n == 0 && p->m > 128 &&
+           pair_tiles >= p->max_pair_clusters;
+  p->pair = pair ? 1 : 0;
+  if (pair) {
+    p->tile_n = 256;
+    p->stages = gf::pair_stages();
+    p->num_n_blocks = static_cast<int>((p->n + 255) / 256);
+    p->num_tiles = static_cast<int>(pair_tiles);
+    const int64_t clusters = pair_tiles < p->max_pair_clusters ? pair_tiles : p->max_pair_clusters;
+    p->grid = static_cast<int>(2 * clusters);
+    return;
+  }
   int tn = p->forced_tile_n;
   if (tn == 0) {
-    // 256-wide tiles halve the operand traffic per flop; take 128 when the
-    // wide tiles would leave SMs idle
+    // 256-wide tiles halve the B traffic per flop; take 128 when the wide
+    // tiles would leave SMs idle
     const int64_t wide = mblocks * ((p->n + 255) / 256);
     tn = wide >= p->num_sms ? 256 : 128;
   }
   p->tile_n = tn;
   p->stages = gf::stages_for(tn);
-  p->num_m_blocks = static_cast<int>(mblocks);
   p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
-  p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
   const int64_t tiles = mblocks * p->num_n_blocks;
   p->num_tiles = static_cast<int>(tiles);
-  p->group_m = 8;
   p->grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
 }
 
@@ -234,6 +258,11 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
   p->wait_limit_ns = 2000000000ull;
   const char* env_tile = getenv("GF_TILE_N");
   p->forced_tile_n = env_tile && (atoi(env_tile) == 128 || atoi(env_tile) == 256) ? atoi(env_tile) : 0;
+  const char* env_kernel = getenv("GF_KERNEL");
+  p->forced_kernel = env_kernel ? atoi(env_kernel) : 0;
+  if (p->forced_kernel < 0 || p->forced_kernel > 2) p->forced_kernel = 0;
+  p->max_pair_clusters = gf::pair_max_clusters_any();
+  cudaGetLastError();
   plan_tiles(p);
 
   if (cudaMalloc(&p->d_status, 256) != cudaSuccess) {
@@ -283,6 +312,12 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       p->forced_tile_n = static_cast<int>(value);
       plan_tiles(p);
       return GF_OK;
+    case GF_OPT_KERNEL:
+      if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
+      if (value == 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
+      p->forced_kernel = static_cast<int>(value);
+      plan_tiles(p);
+      return GF_OK;
     case GF_OPT_FAULT_DROP_LOAD:
       if (value < 0 || value > kMaxDim) return fail(GF_ERR_INVALID_VALUE);
       p->drop_load = static_cast<int>(value);
@@ -294,7 +329,7 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
 GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* tile_n,
                                   int32_t* stages, int32_t* grid, int64_t* workspace_bytes) {
   if (!p) return fail(GF_ERR_INVALID_VALUE);
-  if (tile_m) *tile_m = kBM;
+  if (tile_m) *tile_m = p->pair ? 2 * kBM : kBM;
   if (tile_n) *tile_n = p->tile_n;
   if (stages) *stages = p->stages;
   if (grid) *grid = p->grid;
@@ -340,7 +375,7 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
     if (!encode_2d(&tmA, A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
     const bool ok = p->b_layout == GF_B_KN
                         ? encode_2d(&tmB, B, p->dtype, p->n, p->k, 64, 64)
-                        : encode_2d(&tmB, B, p->dtype, p->k, p->n, 64, p->tile_n);
+                        : encode_2d(&tmB, B, p->dtype, p->k, p->n, 64, p->pair ? 128 : p->tile_n);
     if (!ok) return fail(GF_ERR_INVALID_VALUE);
   }
 
@@ -379,6 +414,7 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
   la.bf16 = p->dtype == GF_BF16 ? 1 : 0;
   la.b_mn = p->b_layout == GF_B_KN ? 1 : 0;
   la.tile_n = p->tile_n;
+  la.pair = p->pair;
   la.stream = st;
 
   cudaError_t err;

@@ -173,13 +173,18 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          stage load, so the consumer's bounded wait runs
  *                          out; execute then completes with
  *                          GF_ERR_DEVICE_TIMEOUT from gf_plan_status. 0: off.
+ * GF_OPT_KERNEL          : 0 the plan's choice, 1 the single-CTA kernel
+ *                          (128 x tile_n tiles), 2 the CTA-pair kernel
+ *                          (256 x 256 tiles on two SMs; GF_ERR_UNSUPPORTED if
+ *                          it cannot be resident on this device).
  * Returns GF_ERR_INVALID_VALUE for an unknown option or value.
  */
 typedef enum gf_option {
   GF_OPT_BGRAD_MODE = 0,
   GF_OPT_WAIT_LIMIT_US = 1,
   GF_OPT_TILE_N = 2,
-  GF_OPT_FAULT_DROP_LOAD = 3
+  GF_OPT_FAULT_DROP_LOAD = 3,
+  GF_OPT_KERNEL = 4
 } gf_option;
 
 GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);

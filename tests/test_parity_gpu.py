@@ -250,25 +250,134 @@ def test_wait_limit_reports_timeout():
     _check_fwd(256, 256, 256, 0, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL, gf.GF_B_KN)
 
 
-def test_one_fused_launch():
+def test_one_fused_launch(tmp_path):
     """One execute = one kernel launch (plus the bgrad finalize for the
-    two-pass backward), counted with the profiler like the SwiGLU sample's
-    launch count (gemm_swiglu_mlp_fusion.py, ``_demo``)."""
+    two-pass backward). Counted from a CUDA graph capture of execute (the
+    SwiGLU sample counts launches too, so that "1 kernel" is shown:
+    gemm_swiglu_mlp_fusion.py, ``_demo``)."""
+    import re
     M, N, K = 512, 512, 256
     A = torch.randn((M, K), device="cuda").half()
     B = torch.randn((K, N), device="cuda").half()
     bias = torch.randn(N, device="cuda").half()
     out = torch.empty((M, N), dtype=torch.float16, device="cuda")
     aux = torch.empty((M // 32, N), dtype=torch.int32, device="cuda")
-    plan = gf.gf_matmul_plan(M, N, K, 0, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
-    gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=aux)
-    torch.cuda.synchronize()
-    with torch.profiler.profile(activities=[torch.profiler.ProfilerActivity.CUDA]) as prof:
-        gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=aux)
+    mask = torch.randint(-2**31, 2**31 - 1, (M // 32, N), dtype=torch.int32, device="cuda")
+    bgrad = torch.empty(N, dtype=torch.float32, device="cuda")
+    fwd = gf.gf_matmul_plan(M, N, K, 0, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    bwd = gf.gf_matmul_plan_ex(M, N, K, 0, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL, gf.GF_B_NK)
+    counts = []
+    for plan, kw in ((fwd, dict(bias=bias, out=out, aux_out=aux)),
+                     (bwd, dict(out=out, aux_in=mask, bgrad=bgrad))):
+        gf.gf_matmul_execute(plan, A, B, **kw)
         torch.cuda.synchronize()
-    names = [e.name for e in prof.events() if str(e.device_type).endswith("CUDA")]
-    names += [e.key for e in prof.key_averages() if e.self_device_time_total > 0]
-    ours = [n for n in names if "gemm_epilog_kernel" in n or "bgrad_finalize" in n]
-    print("profiled device events:", names)
-    assert len(set(ours)) == 1 and sum(1 for n in names if n == ours[0]) >= 1, names
+        g = torch.cuda.CUDAGraph()
+        g.enable_debug_mode()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                gf.gf_matmul_execute(plan, A, B, **kw, stream=s)
+        dot = tmp_path / "g.dot"
+        g.debug_dump(str(dot))
+        text = dot.read_text()
+        nodes = re.findall(r'"(\w+_node_\d+)"\s*\[(.*?)\]\s*;?\s*$', text, re.S | re.M)
+        names = []
+        for _, attrs in nodes:
+            hit = re.search(r"(gemm_epilog\w*?kernel|bgrad_finalize_kernel)", attrs)
+            if hit:
+                names.append(hit.group(1))
+        counts.append(len(names))
+        g.replay()
+        torch.cuda.synchronize()
+        names = sorted(set(names))
+        if plan is fwd:
+            assert names == ["gemm_epilog_kernel"] or names == ["gemm_epilog_pair_kernel"], names
+        else:
+            assert "bgrad_finalize_kernel" in names, names
+    assert counts == [1, 2], counts
+    fwd.free()
+    bwd.free()
+
+
+# ------------------------------------------------------------- CTA-pair kernel
+PAIR_SHAPES = [
+    (256, 256, 64),     # one pair tile
+    (300, 520, 200),    # the second CTA's rows partly past M; ragged N and K
+    (129, 264, 136),    # the peer CTA entirely past M
+    (2048, 2048, 512),  # more pair tiles than resident pairs
+]
+
+
+def _force_pair(plan):
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    assert gf.gf_plan_describe(plan)["tile_m"] == 256
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+@pytest.mark.parametrize("layout", [gf.GF_B_KN, gf.GF_B_NK])
+@pytest.mark.parametrize("epilog,axis", [
+    (gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL), (gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_ROW),
+    (gf.GF_EPILOG_NONE, gf.GF_BIAS_COL),
+])
+def test_pair_forward(M, N, K, layout, epilog, axis):
+    dtype = 0 if K != 200 else 1
+    A, B, bias = _inputs(M, N, K, dtype, layout, 1, bias_len=M if axis == gf.GF_BIAS_ROW else N)
+    tdt = torch_dtype(dtype)
+    out = torch.empty((M, N), dtype=tdt, device="cuda")
+    aux = torch.zeros(((M + 31) // 32, N), dtype=torch.int32, device="cuda")
+    plan = gf.gf_matmul_plan_ex(M, N, K, dtype, epilog, axis, layout)
+    _force_pair(plan)
+    gf.gf_matmul_execute(plan, to_dev(A, dtype), to_dev(B, dtype), bias=to_dev(bias, dtype),
+                         out=out, aux_out=aux if epilog == gf.GF_EPILOG_RELU_AUX_BIAS else None)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    acc = oracle.gemm(A, B, dtype, layout)
+    if epilog == gf.GF_EPILOG_NONE:
+        ref, z = oracle.round_to(acc, dtype), acc
+    else:
+        z = oracle.add_bias(acc, bias, dtype, axis)
+        ref = oracle.round_to(oracle.relu(z), dtype)
+    assert_close(to_host_f32(out), oracle.decode(ref, dtype), what=f"pair out {M}x{N}x{K}")
+    if epilog == gf.GF_EPILOG_RELU_AUX_BIAS:
+        outside, _ = mask_mismatch(unpack_words(to_host_words(aux), M), z)
+        assert outside == 0
+    plan.free()
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+@pytest.mark.parametrize("mode", [gf.GF_BGRAD_TWO_PASS, gf.GF_BGRAD_ATOMIC])
+def test_pair_drelu_bgrad(M, N, K, mode):
+    dtype = 0
+    dY = synth.normal((M, K), dtype, 4, synth.TID_DY, 1.0)
+    W = synth.normal((N, K), dtype, 4, synth.TID_B, 1 / np.sqrt(K))
+    words = synth.mask_words(M, N, 4)
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    bgrad = torch.full((N,), float("nan"), dtype=torch.float32, device="cuda")
+    plan = gf.gf_matmul_plan_ex(M, N, K, dtype, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                gf.GF_B_NK)
+    _force_pair(plan)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_BGRAD_MODE, mode)
+    gf.gf_matmul_execute(plan, to_dev(dY, 0), to_dev(W, 0), out=out, aux_in=to_dev(words, 0),
+                         bgrad=bgrad)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    dz_o, bgrad_o, _ = oracle.drelu_bgrad(dY, W, words, dtype, gf.GF_B_NK)
+    assert_close(to_host_f32(out), oracle.decode(dz_o, 0), what="pair dZ")
+    assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="pair bgrad")
+    plan.free()
+
+
+def test_pair_wait_limit_reports_timeout():
+    M, N, K = 512, 512, 256
+    A, B, bias = _inputs(M, N, K, 0, gf.GF_B_KN, 0)
+    plan = gf.gf_matmul_plan(M, N, K, 0, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL)
+    _force_pair(plan)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_WAIT_LIMIT_US, 20000)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 2)
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    gf.gf_matmul_execute(plan, to_dev(A, 0), to_dev(B, 0), bias=to_dev(bias, 0), out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_ERR_DEVICE_TIMEOUT
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 0)
+    gf.gf_matmul_execute(plan, to_dev(A, 0), to_dev(B, 0), bias=to_dev(bias, 0), out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    z = oracle.add_bias(oracle.gemm(A, B, 0), bias, 0, 0)
+    assert_close(to_host_f32(out), oracle.decode(oracle.round_to(oracle.relu(z), 0), 0))
     plan.free()
