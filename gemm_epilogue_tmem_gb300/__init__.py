@@ -25,7 +25,8 @@ __all__ = [
     "GF_OPT_KERNEL",
     "GfError", "Plan", "build", "lib", "gf_matmul_plan", "gf_matmul_plan_ex",
     "gf_matmul_execute", "gf_plan_status", "gf_plan_set_option", "gf_plan_describe",
-    "gf_plan_free", "gf_status_string", "gf_last_error",
+    "gf_plan_free", "gf_status_string", "gf_last_error", "gf_drelu_bgrad_noalloc",
+    "GF_NOALLOC_MAX_PARTIALS",
 ]
 
 # gf_status
@@ -43,6 +44,8 @@ GF_BGRAD_TWO_PASS, GF_BGRAD_ATOMIC = 0, 1
 # gf_option
 GF_OPT_BGRAD_MODE, GF_OPT_WAIT_LIMIT_US, GF_OPT_TILE_N, GF_OPT_FAULT_DROP_LOAD = 0, 1, 2, 3
 GF_OPT_KERNEL = 4
+# fp32 partial sums the allocation-free DRELU_BGRAD entry point can hold
+GF_NOALLOC_MAX_PARTIALS = 2097152
 
 
 class GfError(RuntimeError):
@@ -84,6 +87,8 @@ def lib(path: str | None = None):
         L.gf_status_string.argtypes = [_I32]
         L.gf_last_error.restype = _I32
         L.gf_last_error.argtypes = []
+        L.gf_drelu_bgrad_noalloc.restype = _I32
+        L.gf_drelu_bgrad_noalloc.argtypes = [_I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]
         _lib = L
     return _lib
 
@@ -184,3 +189,12 @@ def gf_plan_describe(plan: Plan) -> dict:
 def gf_plan_free(plan: Plan) -> None:
     plan.free()
 
+
+def gf_drelu_bgrad_noalloc(m: int, n: int, k: int, dtype: int, b_layout: int, A, B, out, aux_in,
+                           bgrad, stream=None) -> None:
+    """DRELU_BGRAD without any device allocation (fixed scratch inside the
+    library; see include/gf.h). Raises GfError on a non-OK status."""
+    rc = lib().gf_drelu_bgrad_noalloc(m, n, k, dtype, b_layout, _ptr(A), _ptr(B), _ptr(out),
+                                      _ptr(aux_in), _ptr(bgrad), _stream(stream))
+    if rc != GF_OK:
+        raise GfError(rc, "gf_drelu_bgrad_noalloc")

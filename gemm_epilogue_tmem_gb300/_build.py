@@ -17,9 +17,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgf.so")
 
-SOURCES = ["runtime.cu", "k_none_bias.cu", "k_relu.cu", "k_drelu.cu"]
+SOURCES = ["runtime.cu", "k_none_bias.cu", "k_relu.cu", "k_drelu.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "gemm_kernel_2sm.cuh", "dispatch.cuh", "launch.h",
-           "params.h"]
+           "params.h", "runtime_internal.h"]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",

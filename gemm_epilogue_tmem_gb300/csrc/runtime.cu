@@ -19,6 +19,7 @@
 #include "gf.h"
 #include "launch.h"
 #include "params.h"
+#include "runtime_internal.h"
 
 struct gf_plan {
   int64_t m, n, k;
@@ -158,6 +159,19 @@ void plan_tiles(gf_plan* p) {
 }
 
 }  // namespace
+
+namespace gf {
+
+// Shared with the other host entry points of the library (runtime_internal.h).
+gf_status runtime_current_device(int* dev) { return current_device(dev); }
+
+bool runtime_encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner,
+                       uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  load_driver_entry_points();
+  return g_encode != nullptr && encode_2d(map, ptr, dt, inner, outer, box_inner, box_outer);
+}
+
+}  // namespace gf
 
 extern "C" {
 

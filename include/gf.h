@@ -194,6 +194,44 @@ GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t val
 GF_API gf_status gf_plan_describe(const gf_plan* plan, int32_t* tile_m, int32_t* tile_n,
                                   int32_t* stages, int32_t* grid, int64_t* workspace_bytes);
 
+/*
+ * DRELU_BGRAD that allocates nothing. The pages have no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc (or any
+ * allocating routine) -- code that must only use memory handed to it, such
+ * as a framework's memory pool, a real-time loop that must not enter the
+ * allocator, or a host API that forbids allocation while it runs. A plan
+ * (gf_matmul_plan_ex) allocates its workspace; this call does not.
+ *
+ * It computes exactly what gf_matmul_execute computes for a
+ * GF_EPILOG_DRELU_BGRAD plan in GF_BGRAD_TWO_PASS mode (same kernels, same
+ * arguments: A, B, out, aux_in, bgrad as documented there) and returns at
+ * once after enqueuing on `stream`.
+ *
+ * Scratch: the per-128-row-block partial sums live in one fixed device array
+ * inside the library, GF_NOALLOC_MAX_PARTIALS fp32 values (8 MiB) plus a
+ * 256-byte status word. Every GPU that loads the library holds it until the
+ * process exits. ceil(m/128) * n must not exceed GF_NOALLOC_MAX_PARTIALS
+ * (else GF_ERR_UNSUPPORTED, nothing enqueued).
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (cudaGetSymbolAddress; no allocation); make that first call before
+ * any stream capture. Every call shares the one array and reuses it as the
+ * previous call left it: calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller. A bounded wait
+ * that gives up inside the kernel is recorded in the array's status word but
+ * is not reported by this call.
+ *
+ * Returns GF_OK, GF_ERR_INVALID_VALUE (bad size, enum, NULL or misaligned
+ * pointer), GF_ERR_UNSUPPORTED (n or k not a multiple of 8, beyond the
+ * scratch limit, not an sm_103 device), GF_ERR_NO_DEVICE or GF_ERR_CUDA.
+ */
+#define GF_NOALLOC_MAX_PARTIALS 2097152
+
+GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtype dtype,
+                                        gf_b_layout b_layout, const void* A, const void* B,
+                                        void* out, const void* aux_in, float* bgrad,
+                                        struct CUstream_st* stream);
+
 /* Release the plan and its workspace ("free" on the nvmath-python / cuBLASLt
  * page, step 3). Caller tensors are untouched. NULL is a no-op. Work already
  * enqueued with the plan must have completed. */
