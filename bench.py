@@ -114,28 +114,42 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- CPU oracle leg
-def oracle_sample(rows_fwd: int, rows_bwd: int, nthreads: int):
-    """Run the CPU oracle on `rows` sampled rows of both GEMMs of one step.
-    Returns (flops done, seconds of oracle work, description)."""
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs():
+    """Host copies of the step's weight, bias and backward mask (generated once)."""
+    if not _ORACLE_INPUTS:
+        t0 = time.time()
+        _ORACLE_INPUTS["W"] = synth.normal((K, N), synth.F16, 0, synth.TID_B, 1 / 128)
+        _ORACLE_INPUTS["bias"] = synth.normal((N,), synth.F16, 0, synth.TID_BIAS, 0.1)
+        _ORACLE_INPUTS["words"] = synth.mask_words(M, K, 0)  # backward mask, [M/32, K]
+        _ORACLE_INPUTS["rows"] = synth.sample_rows(M, 64, 0)
+        _ORACLE_INPUTS["gen_s"] = time.time() - t0
+    return _ORACLE_INPUTS
+
+
+def oracle_sample(rows_fwd: int, rows_bwd: int, nthreads: int, offset: int = 0):
+    """Run the CPU oracle on sampled rows of both GEMMs of one step (full N,
+    full K). Returns (flops done, seconds of oracle work, description)."""
     import oracle
-    t_gen0 = time.time()
-    W = synth.normal((K, N), synth.F16, 0, synth.TID_B, 1 / 128)
-    bias = synth.normal((N,), synth.F16, 0, synth.TID_BIAS, 0.1)
-    rows = synth.sample_rows(M, 64, 0)
-    rf, rb = rows[:rows_fwd], rows[:rows_bwd]
+    inp = _oracle_inputs()
+    rows = inp["rows"]
+    rf = np.roll(rows, -offset)[:rows_fwd]
+    rb = np.roll(rows, -offset)[:rows_bwd]
     X = synth.normal((M, K), synth.F16, 0, synth.TID_A, 1.0, rows=rf)
     dY = synth.normal((M, N), synth.F16, 0, synth.TID_DY, 1.0, rows=rb)
-    words = synth.mask_words(M, K, 0)  # Bernoulli(1/2) mask of the backward, [M/32, K]
-    gen_s = time.time() - t_gen0
     t0 = time.time()
-    oracle.relu_bias(X, W, bias, oracle.F16, oracle.B_KN, oracle.BIAS_COL, row_ids=rf,
-                     nthreads=nthreads)
+    oracle.relu_bias(X, inp["W"], inp["bias"], oracle.F16, oracle.B_KN, oracle.BIAS_COL,
+                     row_ids=rf, nthreads=nthreads)
     # backward: dY . W^T, W [K, N] being the [n, k] storage of B = W^T
-    oracle.drelu_bgrad(dY, W, words, oracle.F16, oracle.B_NK, row_ids=rb, nthreads=nthreads)
+    oracle.drelu_bgrad(dY, inp["W"], inp["words"], oracle.F16, oracle.B_NK, row_ids=rb,
+                       nthreads=nthreads)
     sec = time.time() - t0
     flops = 2.0 * len(rf) * N * K + 2.0 * len(rb) * K * N
     desc = (f"{len(rf)} sampled rows of the forward and {len(rb)} of the backward GEMM + epilogue "
-            f"(full N, full K), {nthreads} threads; input generation {gen_s:.1f}s not timed")
+            f"(full N, full K) per sample, {nthreads} threads; host input generation "
+            f"({inp['gen_s']:.1f}s) not timed")
     return flops, sec, desc
 
 
@@ -144,13 +158,13 @@ def run_reference(args):
     if rank != 0:
         return 0
     nthreads = os.cpu_count() or 1
-    per_step_rows = max(1, args.ref_rows)
+    per_step_rows = max(1, args.ref_step_rows)
     for _ in range(args.warmup):
         oracle_sample(1, 1, nthreads)
     times, flops_tot = [], 0.0
     desc = ""
-    for _ in range(args.steps):
-        fl, sec, desc = oracle_sample(per_step_rows, per_step_rows, nthreads)
+    for i in range(args.steps):
+        fl, sec, desc = oracle_sample(per_step_rows, per_step_rows, nthreads, offset=i)
         times.append(sec)
         flops_tot += fl
     total = sum(times)
@@ -260,26 +274,30 @@ def run_gpu(args):
         ms_total = float(tt.item())
 
     # epilogue overhead: the same kernels and tiles with no epilogue
-    def time_plan(fn, reps):
-        for _ in range(2):
-            fn()
-        torch.cuda.synchronize()
+    # interleaved, so that clock and power drift hit both variants alike
+    def one(fn):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(reps):
-            fn()
+        fn()
         b.record(stream)
         torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
+        return a.elapsed_time(b)
 
-    reps = max(2, min(args.steps, 5))
-    t_fwd_none = time_plan(lambda: gf.gf_matmul_execute(fwd_none, X, W, out=Y, stream=sp), reps)
-    t_fwd_epi = time_plan(lambda: gf.gf_matmul_execute(fwd, X, W, bias=bias, out=Y, aux_out=aux,
-                                                       stream=sp), reps)
-    t_bwd_none = time_plan(lambda: gf.gf_matmul_execute(bwd_none, dY, W, out=dZ, stream=sp), reps)
-    t_bwd_epi = time_plan(lambda: gf.gf_matmul_execute(bwd, dY, W, out=dZ, aux_in=mask,
-                                                       bgrad=bgrad, stream=sp), reps)
+    f_none = lambda: gf.gf_matmul_execute(fwd_none, X, W, out=Y, stream=sp)  # noqa: E731
+    f_epi = lambda: gf.gf_matmul_execute(fwd, X, W, bias=bias, out=Y, aux_out=aux,  # noqa: E731
+                                         stream=sp)
+    b_none = lambda: gf.gf_matmul_execute(bwd_none, dY, W, out=dZ, stream=sp)  # noqa: E731
+    b_epi = lambda: gf.gf_matmul_execute(bwd, dY, W, out=dZ, aux_in=mask, bgrad=bgrad,  # noqa: E731
+                                         stream=sp)
+    samples = {"fn": [], "fe": [], "bn": [], "be": []}
+    for _ in range(max(3, min(args.steps, 7))):
+        samples["fn"].append(one(f_none))
+        samples["fe"].append(one(f_epi))
+        samples["bn"].append(one(b_none))
+        samples["be"].append(one(b_epi))
+    t_fwd_none, t_fwd_epi = statistics.median(samples["fn"]), statistics.median(samples["fe"])
+    t_bwd_none, t_bwd_epi = statistics.median(samples["bn"]), statistics.median(samples["be"])
 
     # end to end through the C ABI from pinned host memory
     e2e = None
@@ -423,8 +441,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gf", choices=["gf", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=8,
-                    help="sampled rows per GEMM in each CPU-oracle sample")
+    ap.add_argument("--ref-rows", type=int, default=64,
+                    help="sampled rows per GEMM in the CPU-oracle baseline of the GPU run")
+    ap.add_argument("--ref-step-rows", type=int, default=4,
+                    help="sampled rows per GEMM in each step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -19,7 +19,7 @@ __all__ = [
     "GF_ERR_OUT_OF_MEMORY", "GF_ERR_DEVICE_TIMEOUT",
     "GF_F16", "GF_BF16",
     "GF_EPILOG_NONE", "GF_EPILOG_RELU_BIAS", "GF_EPILOG_RELU_AUX_BIAS", "GF_EPILOG_DRELU_BGRAD",
-    "GF_EPILOG_BIAS",
+    "GF_EPILOG_BIAS", "GF_EPILOG_GELU_BIAS", "GF_EPILOG_GELU_AUX_BIAS", "GF_EPILOG_DGELU_BGRAD",
     "GF_BIAS_COL", "GF_BIAS_ROW", "GF_B_KN", "GF_B_NK", "GF_BGRAD_TWO_PASS", "GF_BGRAD_ATOMIC",
     "GF_OPT_BGRAD_MODE", "GF_OPT_WAIT_LIMIT_US", "GF_OPT_TILE_N", "GF_OPT_FAULT_DROP_LOAD",
     "GF_OPT_KERNEL",
@@ -37,6 +37,7 @@ GF_F16, GF_BF16 = 0, 1
 # gf_epilog
 GF_EPILOG_NONE, GF_EPILOG_RELU_BIAS, GF_EPILOG_RELU_AUX_BIAS = 0, 1, 2
 GF_EPILOG_DRELU_BGRAD, GF_EPILOG_BIAS = 3, 4
+GF_EPILOG_GELU_BIAS, GF_EPILOG_GELU_AUX_BIAS, GF_EPILOG_DGELU_BGRAD = 5, 6, 7
 # gf_bias_axis, gf_b_layout, gf_bgrad_mode
 GF_BIAS_COL, GF_BIAS_ROW = 0, 1
 GF_B_KN, GF_B_NK = 0, 1

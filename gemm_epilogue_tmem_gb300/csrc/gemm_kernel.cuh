@@ -89,6 +89,20 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
   for (int i = 0; i < 8; ++i) f[i] = to_f32<T>(h[i]);
 }
 
+// tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear Units",
+// 2016): 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))), and its derivative.
+__device__ __forceinline__ float gelu_tanh(float z) {
+  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+  return 0.5f * z * (1.f + tanhf(u));
+}
+
+__device__ __forceinline__ float dgelu_tanh(float z) {
+  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+  const float t = tanhf(u);
+  return 0.5f * (1.f + t) +
+         0.5f * z * (1.f - t * t) * 0.7978845608028654f * (1.f + 3.f * 0.044715f * z * z);
+}
+
 // Tile t -> (m block, n block): groups of group_m row blocks are swept
 // column by column so that CTAs running together share A and B in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
@@ -119,7 +133,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   const bool wrow_ok = row0 + 32 * q < p.M;
   const T* bias = reinterpret_cast<const T*>(p.bias);
   float row_bias = 0.f;
-  if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS || EPI == EPI_BIAS) {
+  if constexpr (epi_has_bias(EPI)) {
     if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
   }
   T* out = reinterpret_cast<T*>(p.out);
@@ -139,7 +153,22 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
     }
 
-    if constexpr (EPI == EPI_DRELU_BGRAD) {
+    if constexpr (EPI == EPI_DGELU_BGRAD) {
+      // saved pre-activation z of this row's 32 columns (T [M, N])
+      const T* zp = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float z8[8];
+        if (row_ok && col0 + 8 * g < p.N) {
+          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(zp + 8 * g)), z8);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) z8[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] * dgelu_tanh(z8[i]);
+      }
+    } else if constexpr (EPI == EPI_DRELU_BGRAD) {
       uint32_t my_word = 0;
       if (wrow_ok && col0 + (int)lane < p.N)
         my_word = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
@@ -181,6 +210,27 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = v[j] > 0.f ? v[j] : 0.f;
       }
+      if constexpr (EPI == EPI_GELU_AUX_BIAS) {
+        // the pre-activation, rounded to T, for the backward
+        if (row_ok) {
+          T* ap = reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + 8 * g < p.N) {
+              uint4 u;
+              u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
+              u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
+              u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
+              u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
+              *reinterpret_cast<uint4*>(ap + 8 * g) = u;
+            }
+          }
+        }
+      }
+      if constexpr (EPI == EPI_GELU_BIAS || EPI == EPI_GELU_AUX_BIAS) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+      }
     }
 
     if (row_ok) {
@@ -198,7 +248,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     }
 
-    if constexpr (EPI == EPI_DRELU_BGRAD) {
+    if constexpr (epi_has_bgrad(EPI)) {
       // transpose-reduce: after 5 halving steps (31 shuffles) lane l
       // holds the sum of column col0 + l over this warp's 32 rows
 #pragma unroll
@@ -405,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
       bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
-      if constexpr (EPI == EPI_DRELU_BGRAD) {
+      if constexpr (epi_has_bgrad(EPI)) {
         // the four warps meet at named barriers below: they must agree
         ok = !named_bar_red_or(1, 128, !ok);
       }
@@ -425,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8u * buf);
 
-      if constexpr (EPI == EPI_DRELU_BGRAD) epilogue_bgrad<BN>(p, red, ep_tid, n0, mb);
+      if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN>(p, red, ep_tid, n0, mb);
     }
   }
 

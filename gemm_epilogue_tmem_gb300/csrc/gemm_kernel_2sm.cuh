@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
       bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
-      if constexpr (EPI == EPI_DRELU_BGRAD) ok = !named_bar_red_or(1, 128, !ok);
+      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
       if (!ok) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
         aborted = true;
@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(tempty_leader);
-      if constexpr (EPI == EPI_DRELU_BGRAD) epilogue_bgrad<BN>(p, red, ep_tid, n0, row0 / kBM);
+      if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
+      if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN>(p, red, ep_tid, n0, row0 / kBM);
     }
   }
 

@@ -24,6 +24,7 @@ struct LaunchArgs {
 cudaError_t launch_none_bias(int epi, const LaunchArgs& a);   // EPI_NONE, EPI_BIAS
 cudaError_t launch_relu(int epi, const LaunchArgs& a);        // EPI_RELU_BIAS, EPI_RELU_AUX_BIAS
 cudaError_t launch_drelu(const LaunchArgs& a);                // EPI_DRELU_BGRAD
+cudaError_t launch_gelu(int epi, const LaunchArgs& a);        // EPI_GELU_BIAS, _AUX_BIAS, EPI_DGELU_BGRAD
 cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
                                   cudaStream_t stream);
 int smem_bytes_for(int tile_n);

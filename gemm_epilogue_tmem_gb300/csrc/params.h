@@ -3,6 +3,12 @@
 
 #include <stdint.h>
 
+#if defined(__CUDACC__)
+#define GF_HD __host__ __device__
+#else
+#define GF_HD
+#endif
+
 namespace gf {
 
 enum Epi : int {
@@ -11,7 +17,18 @@ enum Epi : int {
   EPI_RELU_AUX_BIAS = 2,
   EPI_DRELU_BGRAD = 3,
   EPI_BIAS = 4,
+  EPI_GELU_BIAS = 5,
+  EPI_GELU_AUX_BIAS = 6,
+  EPI_DGELU_BGRAD = 7,
 };
+
+// epilogs that reduce a bias gradient over the rows of each tile
+GF_HD constexpr bool epi_has_bgrad(int epi) { return epi == EPI_DRELU_BGRAD || epi == EPI_DGELU_BGRAD; }
+// epilogs that add a bias
+GF_HD constexpr bool epi_has_bias(int epi) {
+  return epi == EPI_RELU_BIAS || epi == EPI_RELU_AUX_BIAS || epi == EPI_BIAS ||
+         epi == EPI_GELU_BIAS || epi == EPI_GELU_AUX_BIAS;
+}
 
 // bits of the device status word
 enum : int {

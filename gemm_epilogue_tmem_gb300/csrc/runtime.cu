@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -98,7 +99,14 @@ gf_status current_device(int* dev) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool needs_bias(gf_epilog e) {
-  return e == GF_EPILOG_RELU_BIAS || e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_BIAS;
+  return e == GF_EPILOG_RELU_BIAS || e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_BIAS ||
+         e == GF_EPILOG_GELU_BIAS || e == GF_EPILOG_GELU_AUX_BIAS;
+}
+
+// epilogs that reduce the bias gradient (per-column sums of the masked product)
+bool has_bgrad(gf_epilog e) { return e == GF_EPILOG_DRELU_BGRAD || e == GF_EPILOG_DGELU_BGRAD; }
+bool needs_aux_out(gf_epilog e) {
+  return e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_GELU_AUX_BIAS;
 }
 
 // 2-D tensor map over a row-major [outer, inner] matrix of 16-bit elements,
@@ -203,7 +211,7 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     fail(GF_ERR_INVALID_VALUE);
     return nullptr;
   }
-  if (epilog < GF_EPILOG_NONE || epilog > GF_EPILOG_BIAS) {
+  if (epilog < GF_EPILOG_NONE || epilog > GF_EPILOG_DGELU_BGRAD) {
     fail(GF_ERR_INVALID_VALUE);
     return nullptr;
   }
@@ -219,7 +227,7 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     fail(GF_ERR_UNSUPPORTED);
     return nullptr;
   }
-  if (epilog == GF_EPILOG_DRELU_BGRAD && bias_axis != GF_BIAS_COL) {
+  if (has_bgrad(epilog) && bias_axis != GF_BIAS_COL) {
     fail(GF_ERR_UNSUPPORTED);
     return nullptr;
   }
@@ -291,7 +299,7 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     fail(GF_ERR_CUDA);
     return nullptr;
   }
-  if (epilog == GF_EPILOG_DRELU_BGRAD && m > 0 && n > 0) {
+  if (has_bgrad(epilog) && m > 0 && n > 0) {
     // sized for the narrowest tile so a later tile option never outgrows it
     p->partial_bytes = static_cast<size_t>((m + kBM - 1) / kBM) * static_cast<size_t>(n) * 4;
     if (cudaMalloc(&p->d_partials, p->partial_bytes) != cudaSuccess) {
@@ -363,12 +371,11 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
     if (p->k > 0 && (!A || !B || !aligned16(A) || !aligned16(B)))
       return fail(GF_ERR_INVALID_VALUE);
     if (needs_bias(e) && (!bias || !aligned16(bias))) return fail(GF_ERR_INVALID_VALUE);
-    if (e == GF_EPILOG_RELU_AUX_BIAS && (!aux_out || !aligned16(aux_out)))
+    if (needs_aux_out(e) && (!aux_out || !aligned16(aux_out)))
       return fail(GF_ERR_INVALID_VALUE);
-    if (e == GF_EPILOG_DRELU_BGRAD && (!aux_in || !aligned16(aux_in)))
-      return fail(GF_ERR_INVALID_VALUE);
+    if (has_bgrad(e) && (!aux_in || !aligned16(aux_in))) return fail(GF_ERR_INVALID_VALUE);
   }
-  if (e == GF_EPILOG_DRELU_BGRAD && p->n > 0 && (!bgrad || !aligned16(bgrad)))
+  if (has_bgrad(e) && p->n > 0 && (!bgrad || !aligned16(bgrad)))
     return fail(GF_ERR_INVALID_VALUE);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -376,7 +383,7 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
 
   if (empty) {
     // nothing to multiply; the bias gradient of zero rows is zero
-    if (e == GF_EPILOG_DRELU_BGRAD && p->n > 0 &&
+    if (has_bgrad(e) && p->n > 0 &&
         cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
       return fail(GF_ERR_CUDA);
     return GF_OK;
@@ -412,8 +419,8 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
   prm.wait_limit_ns = p->wait_limit_ns;
   prm.drop_load = p->drop_load;
 
-  const bool atomic = e == GF_EPILOG_DRELU_BGRAD && p->bgrad_mode == GF_BGRAD_ATOMIC;
-  if (e == GF_EPILOG_DRELU_BGRAD) {
+  const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
+  if (has_bgrad(e)) {
     prm.bgrad_atomic = atomic ? 1 : 0;
     prm.bgrad = atomic ? bgrad : p->d_partials;
     if (atomic && cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
@@ -438,10 +445,13 @@ GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* 
     case GF_EPILOG_RELU_BIAS: err = gf::launch_relu(gf::EPI_RELU_BIAS, la); break;
     case GF_EPILOG_RELU_AUX_BIAS: err = gf::launch_relu(gf::EPI_RELU_AUX_BIAS, la); break;
     case GF_EPILOG_DRELU_BGRAD: err = gf::launch_drelu(la); break;
+    case GF_EPILOG_GELU_BIAS: err = gf::launch_gelu(gf::EPI_GELU_BIAS, la); break;
+    case GF_EPILOG_GELU_AUX_BIAS: err = gf::launch_gelu(gf::EPI_GELU_AUX_BIAS, la); break;
+    case GF_EPILOG_DGELU_BGRAD: err = gf::launch_gelu(gf::EPI_DGELU_BGRAD, la); break;
     default: return fail(GF_ERR_INVALID_VALUE);
   }
   if (err != cudaSuccess) return fail(GF_ERR_CUDA);
-  if (e == GF_EPILOG_DRELU_BGRAD && !atomic) {
+  if (has_bgrad(e) && !atomic) {
     err = gf::launch_bgrad_finalize(p->d_partials, p->num_m_blocks, static_cast<int>(p->n), bgrad,
                                     st);
     if (err != cudaSuccess) return fail(GF_ERR_CUDA);
@@ -458,6 +468,9 @@ GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {
   if (cudaMemcpy(&word, p->d_status, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
     return fail(GF_ERR_CUDA);
   if (word != 0) {
+    // which waits gave up: 1 producer, 2 MMA on a stage, 4 MMA on an
+    // accumulator buffer, 8 epilogue, 16 teardown drain
+    if (getenv("GF_DEBUG")) fprintf(stderr, "gf: device status word 0x%x\n", word);
     if (cudaMemset(p->d_status, 0, 4) != cudaSuccess) return fail(GF_ERR_CUDA);
     return fail(GF_ERR_DEVICE_TIMEOUT);
   }

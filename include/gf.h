@@ -76,8 +76,15 @@ typedef enum gf_epilog {
   GF_EPILOG_RELU_BIAS = 1,     /* out = max(acc + bias, 0)                       */
   GF_EPILOG_RELU_AUX_BIAS = 2, /* RELU_BIAS, and aux_out = relu_aux words        */
   GF_EPILOG_DRELU_BGRAD = 3,   /* out = acc masked by aux_in; bgrad = colsum(out) */
-  GF_EPILOG_BIAS = 4           /* out = acc + bias                               */
+  GF_EPILOG_BIAS = 4,          /* out = acc + bias                               */
+  GF_EPILOG_GELU_BIAS = 5,     /* out = gelu(acc + bias), tanh form              */
+  GF_EPILOG_GELU_AUX_BIAS = 6, /* GELU_BIAS, and aux_out = acc + bias (dtype)    */
+  GF_EPILOG_DGELU_BGRAD = 7    /* out = acc * gelu'(aux_in); bgrad = colsum(out) */
 } gf_epilog;
+/* GELU is the tanh form 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+ * (Hendrycks & Gimpel 2016), named as GELU_BIAS on the nvmath-python /
+ * cuBLASLt page ("other epilogs"). Its aux is the pre-activation z = acc +
+ * bias rounded to dtype, [m, n] row-major: what DGELU_BGRAD reads back. */
 
 typedef enum gf_bias_axis {
   GF_BIAS_COL = 0, /* bias[n]: one value per output column, broadcast down rows */
@@ -132,19 +139,23 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
  * Enqueue the planned GEMM + epilogue on `stream` and return at once (the
  * nvmath-python / cuBLASLt page, step 3: execution does not block; the
  * caller synchronises). One kernel launch, plus one small finalize launch
- * for DRELU_BGRAD in GF_BGRAD_TWO_PASS mode.
+ * for DRELU_BGRAD / DGELU_BGRAD in GF_BGRAD_TWO_PASS mode.
  *
  * A       : device [m, k].
  * B       : device [k, n] (GF_B_KN) or [n, k] (GF_B_NK).
  * bias    : device, n (GF_BIAS_COL) or m (GF_BIAS_ROW) elements of dtype.
- *           Required by RELU_BIAS, RELU_AUX_BIAS and BIAS; ignored otherwise.
+ *           Required by RELU_BIAS, RELU_AUX_BIAS, BIAS, GELU_BIAS and
+ *           GELU_AUX_BIAS; ignored otherwise.
  * out     : device [m, n] of dtype. Always required (when m*n > 0).
- * aux_in  : device relu_aux words [ceil(m/32), n] from a RELU_AUX_BIAS
- *           forward. Required by DRELU_BGRAD; ignored otherwise.
- * aux_out : device relu_aux words [ceil(m/32), n], written in full.
- *           Required by RELU_AUX_BIAS; ignored otherwise.
- * bgrad   : device fp32 [n], overwritten with the column sums of the masked
- *           fp32 product. Required by DRELU_BGRAD; ignored otherwise.
+ * aux_in  : DRELU_BGRAD: relu_aux words [ceil(m/32), n] from a RELU_AUX_BIAS
+ *           forward. DGELU_BGRAD: the pre-activation [m, n] of dtype from a
+ *           GELU_AUX_BIAS forward. Required by both; ignored otherwise.
+ * aux_out : RELU_AUX_BIAS: relu_aux words [ceil(m/32), n], written in full.
+ *           GELU_AUX_BIAS: the pre-activation [m, n] of dtype. Required by
+ *           both; ignored otherwise.
+ * bgrad   : device fp32 [n], overwritten with the column sums of the fp32
+ *           epilogue output (before rounding). Required by DRELU_BGRAD and
+ *           DGELU_BGRAD; ignored otherwise.
  * A missing required pointer or a pointer not 16-byte aligned gives
  * GF_ERR_INVALID_VALUE; a failed launch gives GF_ERR_CUDA. The plan's
  * workspace is shared by its calls: use one plan from one stream at a time.

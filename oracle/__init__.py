@@ -84,6 +84,14 @@ def lib():
         L.oracle_mask_bit.argtypes = [_P, _I64, _I64, _I64]
         L.oracle_drelu.argtypes = [_P, _I64, _I64, _P, _P, _P]
         L.oracle_colsum.argtypes = [_P, _I64, _I64, _P]
+        L.oracle_gelu_tanh.restype = ctypes.c_double
+        L.oracle_gelu_tanh.argtypes = [ctypes.c_double]
+        L.oracle_dgelu_tanh.restype = ctypes.c_double
+        L.oracle_dgelu_tanh.argtypes = [ctypes.c_double]
+        L.oracle_gelu.argtypes = [_P, _I64, _P]
+        L.oracle_dgelu.argtypes = [_P, _P, _I64, _P]
+        L.oracle_gelu.restype = None
+        L.oracle_dgelu.restype = None
         for name in ("oracle_decode", "oracle_round", "oracle_gemm_f32", "oracle_gemm_f64",
                      "oracle_add_bias", "oracle_relu", "oracle_relu_bits", "oracle_pack_mask",
                      "oracle_drelu", "oracle_colsum"):
@@ -259,4 +267,58 @@ def drelu_bgrad(G_A, G_B, words, dtype, b_layout=B_NK, row_ids=None, nthreads=No
     dz = drelu(g, words, row_ids)
     out = round_to(dz, dtype)
     bgrad = colsum(dz).astype(np.float32) if row_ids is None else None
+    return out, bgrad, g
+
+
+# ------------------------------------------------------------------ GELU
+def gelu_scalar(z: float) -> float:
+    return float(lib().oracle_gelu_tanh(z))
+
+
+def dgelu_scalar(z: float) -> float:
+    return float(lib().oracle_dgelu_tanh(z))
+
+
+def gelu(z: np.ndarray) -> np.ndarray:
+    """tanh-form GELU (Hendrycks & Gimpel 2016), in double, stored as fp32."""
+    z = _c(z, np.float32)
+    y = np.empty_like(z)
+    lib().oracle_gelu(z.ctypes.data, z.size, y.ctypes.data)
+    return y
+
+
+def dgelu(g: np.ndarray, z: np.ndarray) -> np.ndarray:
+    """dz = g * gelu'(z) (double, stored as fp32)."""
+    g = _c(g, np.float32)
+    z = _c(z, np.float32)
+    assert g.shape == z.shape
+    dz = np.empty_like(g)
+    lib().oracle_dgelu(g.ctypes.data, z.ctypes.data, g.size, dz.ctypes.data)
+    return dz
+
+
+def gelu_bias(A, B, bias, dtype, b_layout=B_KN, axis=BIAS_COL, row_ids=None, nthreads=None):
+    """GELU_BIAS (nvmath-python / cuBLASLt page, "other epilogs"):
+    Y = round(GELU(A B + bias)). Returns (Y bits, z fp32)."""
+    acc = gemm(A, B, dtype, b_layout, nthreads)
+    z = add_bias(acc, bias, dtype, axis, row_ids)
+    return round_to(gelu(z), dtype), z
+
+
+def gelu_aux_bias(A, B, bias, dtype, b_layout=B_KN, axis=BIAS_COL, row_ids=None, nthreads=None):
+    """GELU_AUX_BIAS: GELU_BIAS plus the pre-activation z saved in the
+    operand dtype for the backward. Returns (Y bits, aux bits, z fp32)."""
+    y, z = gelu_bias(A, B, bias, dtype, b_layout, axis, row_ids, nthreads)
+    return y, round_to(z, dtype), z
+
+
+def dgelu_bgrad(G_A, G_B, aux, dtype, b_layout=B_NK, full_rows=True, nthreads=None):
+    """DGELU_BGRAD: g = G_A G_B; dz = g * gelu'(z) with z the saved
+    pre-activation (aux bits of dtype, same rows as G_A); out = round(dz);
+    bgrad = column sums of dz over the batch (when all rows are given)."""
+    g = gemm(G_A, G_B, dtype, b_layout, nthreads)
+    z = decode(aux, dtype)
+    dz = dgelu(g, z)
+    out = round_to(dz, dtype)
+    bgrad = colsum(dz).astype(np.float32) if full_rows else None
     return out, bgrad, g

@@ -283,3 +283,35 @@ void oracle_colsum(const float* dz, int64_t M, int64_t N, double* out) {
   for (int64_t i = 0; i < M; ++i)
     for (int64_t j = 0; j < N; ++j) out[j] += (double)dz[i * N + j];
 }
+
+/* ------------------------------------------------------------ GELU epilogs */
+/* [P2] "other epilogs": GELU_BIAS = GELU(acc + bias). The tanh form of GELU
+ * (Hendrycks & Gimpel, "Gaussian Error Linear Units", 2016, eq. for the tanh
+ * approximation): gelu(z) = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))).
+ * Evaluated in double from the fp32 pre-activation. */
+#define OR_GELU_K0 0.7978845608028654 /* sqrt(2/pi) */
+#define OR_GELU_K1 0.044715
+
+double oracle_gelu_tanh(double z) {
+  double u = OR_GELU_K0 * (z + OR_GELU_K1 * z * z * z);
+  return 0.5 * z * (1.0 + tanh(u));
+}
+
+/* d/dz of the tanh-form GELU:
+ * 0.5 (1 + t) + 0.5 z (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2), t = tanh(u). */
+double oracle_dgelu_tanh(double z) {
+  double u = OR_GELU_K0 * (z + OR_GELU_K1 * z * z * z);
+  double t = tanh(u);
+  return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * OR_GELU_K0 * (1.0 + 3.0 * OR_GELU_K1 * z * z);
+}
+
+/* y = (float) gelu(z) elementwise */
+void oracle_gelu(const float* z, int64_t n, float* y) {
+  for (int64_t i = 0; i < n; ++i) y[i] = (float)oracle_gelu_tanh((double)z[i]);
+}
+
+/* dz = (float) (g * gelu'(z)) elementwise: the GELU backward applied to the
+ * product with the transposed weight, z being the saved pre-activation. */
+void oracle_dgelu(const float* g, const float* z, int64_t n, float* dz) {
+  for (int64_t i = 0; i < n; ++i) dz[i] = (float)((double)g[i] * oracle_dgelu_tanh((double)z[i]));
+}

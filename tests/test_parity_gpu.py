@@ -126,6 +126,7 @@ SHAPES = [
     (33, 8, 8),         # tiny
     (129, 264, 136),
     (4096, 1024, 512),  # more tiles than SMs
+    (4096, 4096, 256),  # 3 to 4 tiles per CTA: both accumulator buffers reused
 ]
 
 
@@ -250,12 +251,35 @@ def test_wait_limit_reports_timeout():
     _check_fwd(256, 256, 256, 0, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL, gf.GF_B_KN)
 
 
-def test_one_fused_launch(tmp_path):
+def _kernel_nodes(graph_handle: int) -> int:
+    """Kernel nodes of a captured CUDA graph, through the CUDA runtime that
+    this process already loaded (the graph is a driver object)."""
+    import ctypes
+    path = None
+    with open("/proc/self/maps") as f:
+        for line in f:
+            if "libcudart.so" in line:
+                path = line.split()[-1]
+                break
+    assert path, "no CUDA runtime loaded"
+    rt = ctypes.CDLL(path)
+    n = ctypes.c_size_t(0)
+    assert rt.cudaGraphGetNodes(ctypes.c_void_p(graph_handle), None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * max(n.value, 1))()
+    assert rt.cudaGraphGetNodes(ctypes.c_void_p(graph_handle), nodes, ctypes.byref(n)) == 0
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert rt.cudaGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kernels += t.value == 0  # cudaGraphNodeTypeKernel
+    return kernels
+
+
+def test_one_fused_launch():
     """One execute = one kernel launch (plus the bgrad finalize for the
     two-pass backward). Counted from a CUDA graph capture of execute (the
     SwiGLU sample counts launches too, so that "1 kernel" is shown:
     gemm_swiglu_mlp_fusion.py, ``_demo``)."""
-    import re
     M, N, K = 512, 512, 256
     A = torch.randn((M, K), device="cuda").half()
     B = torch.randn((K, N), device="cuda").half()
@@ -271,29 +295,17 @@ def test_one_fused_launch(tmp_path):
                      (bwd, dict(out=out, aux_in=mask, bgrad=bgrad))):
         gf.gf_matmul_execute(plan, A, B, **kw)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        g.enable_debug_mode()
+        ref = out.clone()
+        g = torch.cuda.CUDAGraph(keep_graph=True)
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
                 gf.gf_matmul_execute(plan, A, B, **kw, stream=s)
-        dot = tmp_path / "g.dot"
-        g.debug_dump(str(dot))
-        text = dot.read_text()
-        nodes = re.findall(r'"(\w+_node_\d+)"\s*\[(.*?)\]\s*;?\s*$', text, re.S | re.M)
-        names = []
-        for _, attrs in nodes:
-            hit = re.search(r"(gemm_epilog\w*?kernel|bgrad_finalize_kernel)", attrs)
-            if hit:
-                names.append(hit.group(1))
-        counts.append(len(names))
-        g.replay()
+        counts.append(_kernel_nodes(g.raw_cuda_graph()))
+        out.zero_()
+        g.replay()  # the captured launch replays to the same result
         torch.cuda.synchronize()
-        names = sorted(set(names))
-        if plan is fwd:
-            assert names == ["gemm_epilog_kernel"] or names == ["gemm_epilog_pair_kernel"], names
-        else:
-            assert "bgrad_finalize_kernel" in names, names
+        assert torch.equal(out, ref)
     assert counts == [1, 2], counts
     fwd.free()
     bwd.free()
@@ -304,7 +316,9 @@ PAIR_SHAPES = [
     (256, 256, 64),     # one pair tile
     (300, 520, 200),    # the second CTA's rows partly past M; ragged N and K
     (129, 264, 136),    # the peer CTA entirely past M
-    (2048, 2048, 512),  # more pair tiles than resident pairs
+    (2048, 2048, 512),  # nearly one pair tile per resident pair
+    (4096, 4096, 256),  # 3 to 4 pair tiles per pair: both accumulator buffers reused
+    (6000, 2056, 328),  # several tiles per pair, ragged everywhere
 ]
 
 
