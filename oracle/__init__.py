@@ -92,6 +92,14 @@ def lib():
         L.oracle_dgelu.argtypes = [_P, _P, _I64, _P]
         L.oracle_gelu.restype = None
         L.oracle_dgelu.restype = None
+        L.oracle_sigmoid.restype = ctypes.c_double
+        L.oracle_sigmoid.argtypes = [ctypes.c_double]
+        L.oracle_silu.restype = ctypes.c_double
+        L.oracle_silu.argtypes = [ctypes.c_double]
+        L.oracle_swiglu.argtypes = [_P, _P, _I64, _P]
+        L.oracle_swiglu.restype = None
+        L.oracle_dswiglu.argtypes = [_P, _P, _P, _I64, _P, _P]
+        L.oracle_dswiglu.restype = None
         for name in ("oracle_decode", "oracle_round", "oracle_gemm_f32", "oracle_gemm_f64",
                      "oracle_add_bias", "oracle_relu", "oracle_relu_bits", "oracle_pack_mask",
                      "oracle_drelu", "oracle_colsum"):
@@ -322,3 +330,55 @@ def dgelu_bgrad(G_A, G_B, aux, dtype, b_layout=B_NK, full_rows=True, nthreads=No
     out = round_to(dz, dtype)
     bgrad = colsum(dz).astype(np.float32) if full_rows else None
     return out, bgrad, g
+
+
+# ---------------------------------------------------------------- SwiGLU
+def sigmoid_scalar(g: float) -> float:
+    return float(lib().oracle_sigmoid(g))
+
+
+def silu_scalar(g: float) -> float:
+    return float(lib().oracle_silu(g))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """h = silu(g) * u (double, stored as fp32)."""
+    g = _c(g, np.float32)
+    u = _c(u, np.float32)
+    assert g.shape == u.shape
+    h = np.empty_like(g)
+    lib().oracle_swiglu(g.ctypes.data, u.ctypes.data, g.size, h.ctypes.data)
+    return h
+
+
+def dswiglu(dh: np.ndarray, g: np.ndarray, u: np.ndarray):
+    """(d_gate, d_up) of h = silu(g) * u applied to dh (double, stored fp32)."""
+    dh = _c(dh, np.float32)
+    g = _c(g, np.float32)
+    u = _c(u, np.float32)
+    assert dh.shape == g.shape == u.shape
+    dg = np.empty_like(dh)
+    du = np.empty_like(dh)
+    lib().oracle_dswiglu(dh.ctypes.data, g.ctypes.data, u.ctypes.data, dh.size, dg.ctypes.data,
+                         du.ctypes.data)
+    return dg, du
+
+
+def swiglu_forward(x, Wg, Wu, dtype, nthreads=None):
+    """The fused gate+up forward of gemm_swiglu_mlp_fusion.py (docstring):
+    g = x Wg^T, u = x Wu^T (Wg, Wu stored [I, H]: B_NK), h = silu(g) * u.
+    Returns (h bits, g bits, u bits, g fp32, u fp32); g and u rounded are
+    what the forward saves for the backward."""
+    g = gemm(x, Wg, dtype, B_NK, nthreads)
+    u = gemm(x, Wu, dtype, B_NK, nthreads)
+    h = round_to(swiglu(g, u), dtype)
+    return h, round_to(g, dtype), round_to(u, dtype), g, u
+
+
+def dswiglu_backward(dout, Wd, g_bits, u_bits, dtype, nthreads=None):
+    """dh = dout Wd (Wd stored [H, I]: B_KN), then the dSwiGLU of the saved
+    g, u as its epilogue (gemm_swiglu_mlp_fusion.py, docstring).
+    Returns (d_gate bits, d_up bits, dh fp32)."""
+    dh = gemm(dout, Wd, dtype, B_KN, nthreads)
+    dg, du = dswiglu(dh, decode(g_bits, dtype), decode(u_bits, dtype))
+    return round_to(dg, dtype), round_to(du, dtype), dh

@@ -315,3 +315,31 @@ void oracle_gelu(const float* z, int64_t n, float* y) {
 void oracle_dgelu(const float* g, const float* z, int64_t n, float* dz) {
   for (int64_t i = 0; i < n; ++i) dz[i] = (float)((double)g[i] * oracle_dgelu_tanh((double)z[i]));
 }
+
+/* ------------------------------------------------------------------ SwiGLU */
+/* [P3] "gemm_swiglu_mlp_fusion.py", module docstring: the forward fuses
+ * silu(x Wg^T) * (x Wu^T) (gate GEMM + up GEMM + SiLU + mul), the down
+ * projection is a separate GEMM, and the backward's dSwiGLU is fused as the
+ * epilogue of matmul(dout, Wd) -> dh. silu(g) = g * sigmoid(g),
+ * sigmoid(g) = 1 / (1 + exp(-g)). Evaluated in double from fp32 inputs. */
+double oracle_sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+double oracle_silu(double g) { return g * oracle_sigmoid(g); }
+
+/* h = (float) (silu(g) * u) elementwise */
+void oracle_swiglu(const float* g, const float* u, int64_t n, float* h) {
+  for (int64_t i = 0; i < n; ++i) h[i] = (float)(oracle_silu((double)g[i]) * (double)u[i]);
+}
+
+/* The derivatives of h = silu(g) * u, applied to dh:
+ *   d_up   = dh * silu(g)
+ *   d_gate = dh * u * sigmoid(g) * (1 + g * (1 - sigmoid(g)))
+ * (d silu / dg = sigmoid(g) + g sigmoid(g) (1 - sigmoid(g))). */
+void oracle_dswiglu(const float* dh, const float* g, const float* u, int64_t n, float* d_gate,
+                    float* d_up) {
+  for (int64_t i = 0; i < n; ++i) {
+    double s = oracle_sigmoid((double)g[i]);
+    d_up[i] = (float)((double)dh[i] * ((double)g[i] * s));
+    d_gate[i] = (float)((double)dh[i] * (double)u[i] * s * (1.0 + (double)g[i] * (1.0 - s)));
+  }
+}
