@@ -26,6 +26,7 @@ __all__ = [
     "GfError", "Plan", "build", "lib", "gf_matmul_plan", "gf_matmul_plan_ex",
     "gf_matmul_execute", "gf_plan_status", "gf_plan_set_option", "gf_plan_describe",
     "gf_plan_free", "gf_status_string", "gf_last_error", "gf_drelu_bgrad_noalloc",
+    "gf_swiglu_plan", "gf_swiglu_execute", "gf_dswiglu_plan", "gf_dswiglu_execute",
     "GF_NOALLOC_MAX_PARTIALS",
 ]
 
@@ -88,6 +89,14 @@ def lib(path: str | None = None):
         L.gf_status_string.argtypes = [_I32]
         L.gf_last_error.restype = _I32
         L.gf_last_error.argtypes = []
+        L.gf_swiglu_plan.restype = _P
+        L.gf_swiglu_plan.argtypes = [_I64, _I64, _I64, _I32, _I32]
+        L.gf_swiglu_execute.restype = _I32
+        L.gf_swiglu_execute.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
+        L.gf_dswiglu_plan.restype = _P
+        L.gf_dswiglu_plan.argtypes = [_I64, _I64, _I64, _I32]
+        L.gf_dswiglu_execute.restype = _I32
+        L.gf_dswiglu_execute.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
         L.gf_drelu_bgrad_noalloc.restype = _I32
         L.gf_drelu_bgrad_noalloc.argtypes = [_I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]
         _lib = L
@@ -164,6 +173,36 @@ def gf_matmul_execute(plan: Plan, A, B, bias=None, out=None, aux_in=None, aux_ou
                                  _ptr(aux_in), _ptr(aux_out), _ptr(bgrad), _stream(stream))
     if rc != GF_OK:
         raise GfError(rc, "gf_matmul_execute")
+
+
+def gf_swiglu_plan(m: int, n: int, k: int, dtype: int, save_gu: bool = False) -> Plan:
+    """Gate+up SwiGLU forward plan: h[m, n] = silu(x Wg^T) * (x Wu^T), x [m, k]."""
+    h = lib().gf_swiglu_plan(m, n, k, dtype, 1 if save_gu else 0)
+    if not h:
+        raise GfError(gf_last_error(), "gf_swiglu_plan")
+    return Plan(h, m, n, k, dtype, -1, GF_BIAS_COL, GF_B_NK)
+
+
+def gf_swiglu_execute(plan: Plan, x, Wg, Wu, h, g_out=None, u_out=None, stream=None) -> None:
+    rc = lib().gf_swiglu_execute(plan.handle, _ptr(x), _ptr(Wg), _ptr(Wu), _ptr(h), _ptr(g_out),
+                                 _ptr(u_out), _stream(stream))
+    if rc != GF_OK:
+        raise GfError(rc, "gf_swiglu_execute")
+
+
+def gf_dswiglu_plan(m: int, n: int, k: int, dtype: int) -> Plan:
+    """dSwiGLU backward plan: dh = dout Wd with the dSwiGLU as its epilogue."""
+    h = lib().gf_dswiglu_plan(m, n, k, dtype)
+    if not h:
+        raise GfError(gf_last_error(), "gf_dswiglu_plan")
+    return Plan(h, m, n, k, dtype, -2, GF_BIAS_COL, GF_B_KN)
+
+
+def gf_dswiglu_execute(plan: Plan, dout, Wd, g, u, d_gate, d_up, stream=None) -> None:
+    rc = lib().gf_dswiglu_execute(plan.handle, _ptr(dout), _ptr(Wd), _ptr(g), _ptr(u),
+                                  _ptr(d_gate), _ptr(d_up), _stream(stream))
+    if rc != GF_OK:
+        raise GfError(rc, "gf_dswiglu_execute")
 
 
 def gf_plan_status(plan: Plan, stream=None) -> int:

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgf.so")
 
-SOURCES = ["runtime.cu", "k_none_bias.cu", "k_relu.cu", "k_drelu.cu", "k_gelu.cu", "noalloc.cu"]
+SOURCES = ["runtime.cu", "k_none_bias.cu", "k_relu.cu", "k_drelu.cu", "k_gelu.cu", "k_swiglu.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "gemm_kernel.cuh", "gemm_kernel_2sm.cuh", "dispatch.cuh", "launch.h",
            "params.h", "runtime_internal.h"]
 

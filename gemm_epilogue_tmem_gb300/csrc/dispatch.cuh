@@ -10,7 +10,7 @@ namespace gf {
 template <int EPI, typename T, bool B_MN, int BN>
 cudaError_t launch_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_kernel<EPI, T, B_MN, BN>;
-  constexpr int smem = TileCfg<BN>::kSmemBytes;
+  constexpr int smem = TileCfg<BN, epi_dual(EPI) ? 2 : 1>::kSmemBytes;
   static bool attr_set = false;  // once per instance and process
   if (!attr_set) {
     cudaError_t e =
@@ -18,14 +18,14 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kernel<<<a.grid, kThreads, smem, a.stream>>>(*a.tmA, *a.tmB, *a.params);
+  kernel<<<a.grid, kThreads, smem, a.stream>>>(*a.tmA, *a.tmB, *a.tmB2, *a.params);
   return cudaGetLastError();
 }
 
 template <int EPI, typename T, bool B_MN>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg::kSmemBytes;
+  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -45,14 +45,14 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.params);
+  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.params);
 }
 
 // Largest number of CTA pairs of this instance that can be resident at once.
 template <int EPI, typename T, bool B_MN>
 int pair_max_clusters() {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg::kSmemBytes;
+  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1>::kSmemBytes;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
@@ -70,6 +70,17 @@ int pair_max_clusters() {
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
   return n;
+}
+
+// two-B-operand epilogs: B given [n, k] (K-major), 128-wide single-CTA tiles or CTA pairs
+template <int EPI>
+cudaError_t launch_dual(const LaunchArgs& a) {
+  if (a.b_mn) return cudaErrorInvalidValue;
+  if (a.pair)
+    return a.bf16 ? launch_pair_instance<EPI, __nv_bfloat16, false>(a)
+                  : launch_pair_instance<EPI, __half, false>(a);
+  return a.bf16 ? launch_instance<EPI, __nv_bfloat16, false, 128>(a)
+                : launch_instance<EPI, __half, false, 128>(a);
 }
 
 template <int EPI>

@@ -44,16 +44,20 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;  // 64 x 16-bit = 128 bytes = one swizzle row
 constexpr int kThreads = 192;
 
-template <int BN>
+// NB = number of B operands (2 for the gate+up SwiGLU: two accumulators)
+template <int BN, int NB = 1>
 struct TileCfg {
   static_assert(BN == 128 || BN == 256, "tile N");
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static_assert(NB == 1 || (NB == 2 && BN == 128), "two B operands need 128-wide tiles");
+  static constexpr int kStages = (BN == 256 || NB == 2) ? 4 : 6;
   static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
+  static constexpr int kBBytes = BN * kBK * 2;            // one B operand
+  static constexpr int kStageBBytes = NB * kBBytes;       // all B operands of a stage
+  static constexpr int kAccCols = NB * BN;                // TMEM columns of one accumulator set
+  static constexpr int kTmemCols = 2 * kAccCols;          // two accumulator buffers
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kRedBytes = 4 * BN * 4;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * (kABytes + kBBytes) +
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes;
 };
 
@@ -103,6 +107,29 @@ __device__ __forceinline__ float dgelu_tanh(float z) {
          0.5f * z * (1.f - t * t) * 0.7978845608028654f * (1.f + 3.f * 0.044715f * z * z);
 }
 
+// SiLU and the logistic function of the SwiGLU epilogues (gate+up
+// forward, dSwiGLU backward): sigmoid(g) = 1 / (1 + e^-g), silu(g) = g sigmoid(g).
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
+
+__device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
+
+// 32 consecutive values of one row -> 4 x 16-byte stores of T (columns at or
+// past N are skipped; N is a multiple of 8)
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const float* v, int col0, int N) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (col0 + 8 * g < N) {
+      uint4 u;
+      u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
+      u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
+      u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
+      u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
+      *reinterpret_cast<uint4*>(dst + 8 * g) = u;
+    }
+  }
+}
+
 // Tile t -> (m block, n block): groups of group_m row blocks are swept
 // column by column so that CTAs running together share A and B in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
@@ -142,18 +169,68 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
     const int col0 = n0 + 32 * c;
     if (col0 >= p.N) break;  // same for every epilogue warp
     float v[32];
+    float u2[epi_dual(EPI) ? 32 : 1];  // the second accumulator (the SwiGLU "up" product)
     if (p.num_k_blocks > 0) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(t_row + 32u * c, r);
-      tmem_ld_wait();
+      if constexpr (epi_dual(EPI)) {
+        uint32_t r2[32];
+        tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * c, r2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u2[j] = __uint_as_float(r2[j]);
+      } else {
+        tmem_ld_wait();
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      if constexpr (epi_dual(EPI)) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u2[j] = 0.f;
+      }
     }
 
-    if constexpr (EPI == EPI_DGELU_BGRAD) {
+    if constexpr (epi_dual(EPI)) {
+      // gate+up SwiGLU: v = g = x Wg^T, u2 = u = x Wu^T; h = silu(g) * u
+      if constexpr (EPI == EPI_SWIGLU_SAVE) {
+        if (row_ok) {
+          store_row32<T>(reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0, v, col0, p.N);
+          store_row32<T>(reinterpret_cast<T*>(p.aux_out2) + (size_t)row * p.N + col0, u2, col0,
+                         p.N);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u2[j];
+    } else if constexpr (EPI == EPI_DSWIGLU) {
+      // v = dh = dout Wd; saved g (aux_in) and u (aux_in2) of this row's 32
+      // columns; out = d_gate, aux_out = d_up
+      const T* gp = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
+      const T* up = reinterpret_cast<const T*>(p.aux_in2) + (size_t)row * p.N + col0;
+      float dup[32];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        float g8[8], u8[8];
+        if (row_ok && col0 + 8 * g < p.N) {
+          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(gp + 8 * g)), g8);
+          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(up + 8 * g)), u8);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) g8[i] = u8[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float s = sigmoid_f(g8[i]);
+          const float dh = v[8 * g + i];
+          dup[8 * g + i] = dh * (g8[i] * s);
+          v[8 * g + i] = dh * u8[i] * s * (1.f + g8[i] * (1.f - s));
+        }
+      }
+      if (row_ok)
+        store_row32<T>(reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0, dup, col0, p.N);
+    } else if constexpr (EPI == EPI_DGELU_BGRAD) {
       // saved pre-activation z of this row's 32 columns (T [M, N])
       const T* zp = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
 #pragma unroll
@@ -290,8 +367,10 @@ __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float*
 template <int EPI, typename T, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilog_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using C = TileCfg<BN>;
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+  constexpr int NB = epi_dual(EPI) ? 2 : 1;
+  using C = TileCfg<BN, NB>;
   constexpr int S = C::kStages;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];
@@ -301,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + S * C::kABytes;
-  const uint32_t ctrl = sB + S * C::kBBytes;
+  const uint32_t ctrl = sB + S * C::kStageBBytes;
   uint8_t* gctrl = gbase + (ctrl - base);
   const uint32_t full0 = ctrl;               // S barriers: stage filled
   const uint32_t empty0 = ctrl + 8u * S;     // S barriers: stage consumed
@@ -330,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.num_k_blocks > 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (NB == 2) prefetch_tmap(&tmB2);
     }
   }
   if (warp == 1) {
@@ -356,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(p, t, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
         const int nbox = B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 1;
-        const uint32_t bytes = C::kABytes + (B_MN ? nbox * 64 * kBK * 2 : C::kBBytes);
+        const uint32_t bytes = C::kABytes + (B_MN ? nbox * 64 * kBK * 2 : C::kStageBBytes);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
@@ -370,10 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0);
             if (B_MN) {
               for (int j = 0; j < nbox; ++j)
-                tma_load_2d(sB + stage * C::kBBytes + j * (64 * kBK * 2), &tmB, fb, n0 + 64 * j,
-                            kb * kBK);
+                tma_load_2d(sB + stage * C::kStageBBytes + j * (64 * kBK * 2), &tmB, fb,
+                            n0 + 64 * j, kb * kBK);
             } else {
-              tma_load_2d(sB + stage * C::kBBytes, &tmB, fb, kb * kBK, n0);
+              tma_load_2d(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n0);
+              if (NB == 2)  // the second B operand right after the first
+                tma_load_2d(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK, n0);
             }
             issued[stage] = (int)phase;
           }
@@ -407,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * C::kAccCols);
         if (p.num_k_blocks == 0) {
           mbar_arrive(tfull0 + 8u * buf);  // acc is all zeros: nothing to multiply
           continue;
@@ -420,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_base = sA + stage * C::kABytes;
-          const uint32_t b_base = sB + stage * C::kBBytes;
+          const uint32_t b_base = sB + stage * C::kStageBBytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             // K-major A: 16 k = 32 bytes along the swizzled 128-byte row;
@@ -431,6 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
             umma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (NB == 2) {  // second accumulator: columns [BN, 2 BN) of the set
+              const uint64_t bdesc2 = sdesc_sw128(b_base + C::kBBytes + kk * 32, 16, 1024);
+              umma_f16(d_tmem + BN, adesc, bdesc2, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(empty0 + 8u * stage);  // frees the stage once these MMAs finish
           if (++stage == S) {
@@ -467,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m0 = mb * kBM, n0 = nb * BN;
-      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN);
+      const uint32_t t_row =
+          tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
 
       epilogue_drain<EPI, T, BN>(p, t_row, m0, n0, q, lane, red);
       // accumulator buffer drained: the MMA warp may reuse it

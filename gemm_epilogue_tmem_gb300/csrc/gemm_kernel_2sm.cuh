@@ -1,6 +1,7 @@
 // CTA-pair variant of the fused GEMM + epilogue kernel: a cluster of two
 // CTAs on two SMs computes one 256 x 256 output tile with
-// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction).
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction); with
+// two B operands (gate+up SwiGLU) a 256 x 128 tile of each, N = 128.
 //
 //   - Each CTA loads its own 128 rows of A and its own 128 columns of B for
 //     every k-slice (TMA, 128-byte swizzle, no multicast): per SM the operand
@@ -20,16 +21,20 @@
 
 namespace gf {
 
+// NB = number of B operands: 1, or 2 for the gate+up SwiGLU (two accumulators)
+template <int NB = 1>
 struct PairCfg {
-  static constexpr int BN = 256;          // pair tile 256 x 256, each CTA 128 x 256
+  static constexpr int BN = NB == 2 ? 128 : 256;       // pair tile 256 x BN per B operand
   static constexpr int kStages = 6;
-  static constexpr int kABytes = kBM * kBK * 2;          // 16 KB: this CTA's 128 rows
-  static constexpr int kBBytes = (BN / 2) * kBK * 2;     // 16 KB: this CTA's 128 columns
-  static constexpr int kTmemCols = 2 * BN;               // two accumulator buffers
+  static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;   // this CTA's BN/2 columns of one B
+  static constexpr int kStageBBytes = NB * kBBytes;    // 16 KB either way
+  static constexpr int kAccCols = NB * BN;             // TMEM columns of one accumulator set
+  static constexpr int kTmemCols = 2 * kAccCols;       // two accumulator buffers
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kRedBytes = 4 * BN * 4;
   static constexpr int kSmemBytes =
-      1024 + kStages * (kABytes + kBBytes) + kCtrlBytes + kRedBytes;
+      1024 + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
 };
 
 // Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
@@ -47,8 +52,10 @@ __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int
 template <int EPI, typename T, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
-  using C = PairCfg;
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+  constexpr int NB = epi_dual(EPI) ? 2 : 1;
+  using C = PairCfg<NB>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -59,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = base + S * C::kABytes;
-  const uint32_t ctrl = sB + S * C::kBBytes;
+  const uint32_t ctrl = sB + S * C::kStageBBytes;
   uint8_t* gctrl = gbase + (ctrl - base);
   const uint32_t full0 = ctrl;              // leader: S barriers, stage filled (both CTAs' bytes)
   const uint32_t empty0 = ctrl + 8u * S;    // both: S barriers, stage consumed
@@ -93,6 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.num_k_blocks > 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
+      if (NB == 2) prefetch_tmap(&tmB2);
     }
   }
   if (warp == 1) {
@@ -119,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
         const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
-        const int n_col = nb * BN + 128 * (int)rank;    // this CTA's B columns
+        const int n_col = nb * BN + (BN / 2) * (int)rank;  // this CTA's B columns
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
@@ -131,14 +139,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (loads != p.drop_load) {
             const uint32_t fb_local = full0 + 8u * stage;
             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
-            if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kBBytes));
+            if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kStageBBytes));
             tma_load_2d_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row);
             if (B_MN) {
-              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, fb, n_col, kb * kBK);
-              tma_load_2d_pair(sB + stage * C::kBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
+              tma_load_2d_pair(sB + stage * C::kStageBBytes, &tmB, fb, n_col, kb * kBK);
+              tma_load_2d_pair(sB + stage * C::kStageBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
                                kb * kBK);
             } else {
-              tma_load_2d_pair(sB + stage * C::kBBytes, &tmB, fb, kb * kBK, n_col);
+              tma_load_2d_pair(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n_col);
+              if (NB == 2)
+                tma_load_2d_pair(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK,
+                                 n_col);
             }
             issued[stage] = (int)phase;
           }
@@ -177,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * C::kAccCols);
         if (p.num_k_blocks == 0) {
           umma_commit_pair(tfull0 + 8u * buf, 0x3);  // nothing to multiply: acc is zero
           continue;
@@ -191,13 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_base = sA + stage * C::kABytes;
-          const uint32_t b_base = sB + stage * C::kBBytes;
+          const uint32_t b_base = sB + stage * C::kStageBBytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
             umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (NB == 2) {
+              const uint64_t bdesc2 = sdesc_sw128(b_base + C::kBBytes + kk * 32, 16, 1024);
+              umma_f16_pair(d_tmem + BN, adesc, bdesc2, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
           if (++stage == S) {
@@ -233,7 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       pair_tile_coords(p, t, mb2, nb);
       const int row0 = mb2 * 256 + 128 * (int)rank;
       const int n0 = nb * BN;
-      const uint32_t t_row = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN);
+      const uint32_t t_row =
+          tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
       tc_fence_before();
       __syncwarp();

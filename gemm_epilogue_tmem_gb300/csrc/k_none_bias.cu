@@ -11,7 +11,7 @@ int smem_bytes_for(int tile_n) {
   return tile_n == 256 ? TileCfg<256>::kSmemBytes : TileCfg<128>::kSmemBytes;
 }
 
-int pair_stages() { return PairCfg::kStages; }
+int pair_stages() { return PairCfg<1>::kStages; }
 
 int pair_max_clusters_any() { return pair_max_clusters<EPI_NONE, __half, false>(); }
 

@@ -12,6 +12,7 @@ namespace gf {
 struct LaunchArgs {
   const CUtensorMap* tmA;
   const CUtensorMap* tmB;
+  const CUtensorMap* tmB2;  // second B operand (SwiGLU up projection); else = tmB
   const GemmParams* params;
   int grid;
   int bf16;     // 0: fp16, 1: bf16
@@ -25,6 +26,7 @@ cudaError_t launch_none_bias(int epi, const LaunchArgs& a);   // EPI_NONE, EPI_B
 cudaError_t launch_relu(int epi, const LaunchArgs& a);        // EPI_RELU_BIAS, EPI_RELU_AUX_BIAS
 cudaError_t launch_drelu(const LaunchArgs& a);                // EPI_DRELU_BGRAD
 cudaError_t launch_gelu(int epi, const LaunchArgs& a);        // EPI_GELU_BIAS, _AUX_BIAS, EPI_DGELU_BGRAD
+cudaError_t launch_swiglu(int epi, const LaunchArgs& a);      // EPI_SWIGLU, _SAVE, EPI_DSWIGLU
 cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
                                   cudaStream_t stream);
 int smem_bytes_for(int tile_n);

@@ -20,7 +20,13 @@ enum Epi : int {
   EPI_GELU_BIAS = 5,
   EPI_GELU_AUX_BIAS = 6,
   EPI_DGELU_BGRAD = 7,
+  EPI_SWIGLU = 8,       // h = silu(x Wg^T) * (x Wu^T): two B operands, two accumulators
+  EPI_SWIGLU_SAVE = 9,  // ... and g, u saved for the backward
+  EPI_DSWIGLU = 10,     // d_gate, d_up of h = silu(g) * u from dh = dout Wd
 };
+
+// epilogs with two B operands (and two accumulators per tile)
+GF_HD constexpr bool epi_dual(int epi) { return epi == EPI_SWIGLU || epi == EPI_SWIGLU_SAVE; }
 
 // epilogs that reduce a bias gradient over the rows of each tile
 GF_HD constexpr bool epi_has_bgrad(int epi) { return epi == EPI_DRELU_BGRAD || epi == EPI_DGELU_BGRAD; }
@@ -48,6 +54,8 @@ struct GemmParams {
   void* out;
   uint32_t* aux_out;
   const uint32_t* aux_in;
+  void* aux_out2;        // SWIGLU_SAVE: u
+  const void* aux_in2;   // DSWIGLU: saved u
   float* bgrad;  // atomic: bgrad[N] (zeroed first); two-pass: partials [num_m_blocks][N]
   int32_t* status;
   uint64_t wait_limit_ns;

@@ -25,7 +25,7 @@
 struct gf_plan {
   int64_t m, n, k;
   gf_dtype dtype;
-  gf_epilog epilog;
+  int epi;               // gf::Epi code (the public gf_epilog values, plus SwiGLU forms)
   gf_bias_axis bias_axis;
   gf_b_layout b_layout;
   int device;
@@ -98,16 +98,15 @@ gf_status current_device(int* dev) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool needs_bias(gf_epilog e) {
-  return e == GF_EPILOG_RELU_BIAS || e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_BIAS ||
-         e == GF_EPILOG_GELU_BIAS || e == GF_EPILOG_GELU_AUX_BIAS;
-}
+bool needs_bias(int e) { return gf::epi_has_bias(e); }
 
-// epilogs that reduce the bias gradient (per-column sums of the masked product)
-bool has_bgrad(gf_epilog e) { return e == GF_EPILOG_DRELU_BGRAD || e == GF_EPILOG_DGELU_BGRAD; }
-bool needs_aux_out(gf_epilog e) {
-  return e == GF_EPILOG_RELU_AUX_BIAS || e == GF_EPILOG_GELU_AUX_BIAS;
+// epilogs that reduce the bias gradient (per-column sums of the epilogue output)
+bool has_bgrad(int e) { return gf::epi_has_bgrad(e); }
+bool needs_aux_out(int e) {
+  return e == gf::EPI_RELU_AUX_BIAS || e == gf::EPI_GELU_AUX_BIAS || e == gf::EPI_SWIGLU_SAVE ||
+         e == gf::EPI_DSWIGLU;
 }
+bool needs_aux_in(int e) { return has_bgrad(e) || e == gf::EPI_DSWIGLU; }
 
 // 2-D tensor map over a row-major [outer, inner] matrix of 16-bit elements,
 // boxes of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
@@ -126,15 +125,17 @@ bool encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner, u
 }
 
 void plan_tiles(gf_plan* p) {
+  const bool dual = gf::epi_dual(p->epi);
   const int64_t mblocks = (p->m + kBM - 1) / kBM;
   p->num_m_blocks = static_cast<int>(mblocks);
   p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
   p->group_m = 8;
-  // The CTA-pair kernel (256 x 256 tiles over two SMs) moves 2/3 of the
-  // operand bytes per flop of the single-CTA 128 x 256 tile; take it when its
-  // tiles fill the resident pairs, else the single-CTA kernel with the tile
-  // width that keeps the SMs busy.
-  const int64_t pair_tiles = ((p->m + 255) / 256) * ((p->n + 255) / 256);
+  // The CTA-pair kernel (256 x 256 tiles over two SMs; 256 x 128 per operand
+  // with two B operands) moves 2/3 of the operand bytes per flop of the
+  // single-CTA tile; take it when its tiles fill the resident pairs, else the
+  // single-CTA kernel with the tile width that keeps the SMs busy.
+  const int pair_n = dual ? 128 : 256;
+  const int64_t pair_tiles = ((p->m + 255) / 256) * ((p->n + pair_n - 1) / pair_n);
   bool pair = false;
   if (p->forced_kernel == 2)
     pair = p->max_pair_clusters > 0;
@@ -143,64 +144,35 @@ void plan_tiles(gf_plan* p) {
            pair_tiles >= p->max_pair_clusters;
   p->pair = pair ? 1 : 0;
   if (pair) {
-    p->tile_n = 256;
+    p->tile_n = pair_n;
     p->stages = gf::pair_stages();
-    p->num_n_blocks = static_cast<int>((p->n + 255) / 256);
+    p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
     const int64_t clusters = pair_tiles < p->max_pair_clusters ? pair_tiles : p->max_pair_clusters;
     p->grid = static_cast<int>(2 * clusters);
     return;
   }
   int tn = p->forced_tile_n;
-  if (tn == 0) {
+  if (dual) {
+    tn = 128;  // two 128-column accumulators per buffer fill the tensor memory
+  } else if (tn == 0) {
     // 256-wide tiles halve the B traffic per flop; take 128 when the wide
     // tiles would leave SMs idle
     const int64_t wide = mblocks * ((p->n + 255) / 256);
     tn = wide >= p->num_sms ? 256 : 128;
   }
   p->tile_n = tn;
-  p->stages = gf::stages_for(tn);
+  p->stages = dual ? 4 : gf::stages_for(tn);
   p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
   const int64_t tiles = mblocks * p->num_n_blocks;
   p->num_tiles = static_cast<int>(tiles);
   p->grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
 }
 
-}  // namespace
-
-namespace gf {
-
-// Shared with the other host entry points of the library (runtime_internal.h).
-gf_status runtime_current_device(int* dev) { return current_device(dev); }
-
-bool runtime_encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner,
-                       uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
-  load_driver_entry_points();
-  return g_encode != nullptr && encode_2d(map, ptr, dt, inner, outer, box_inner, box_outer);
-}
-
-}  // namespace gf
-
-extern "C" {
-
-GF_API const char* gf_status_string(gf_status s) {
-  switch (s) {
-    case GF_OK: return "GF_OK";
-    case GF_ERR_INVALID_VALUE: return "GF_ERR_INVALID_VALUE: invalid argument";
-    case GF_ERR_UNSUPPORTED: return "GF_ERR_UNSUPPORTED: valid but not supported";
-    case GF_ERR_NO_DEVICE: return "GF_ERR_NO_DEVICE: no CUDA device";
-    case GF_ERR_CUDA: return "GF_ERR_CUDA: a CUDA call failed";
-    case GF_ERR_OUT_OF_MEMORY: return "GF_ERR_OUT_OF_MEMORY: workspace allocation failed";
-    case GF_ERR_DEVICE_TIMEOUT: return "GF_ERR_DEVICE_TIMEOUT: a bounded wait in a kernel gave up";
-  }
-  return "unknown gf_status";
-}
-
-GF_API gf_status gf_last_error(void) { return g_last; }
-
-GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtype,
-                                  gf_epilog epilog, gf_bias_axis bias_axis,
-                                  gf_b_layout b_layout) {
+// Validation, device checks, tile choice and workspace: the plan step of
+// every public plan constructor. epi is a gf::Epi code.
+gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
+                     gf_bias_axis bias_axis, gf_b_layout b_layout) {
   g_last = GF_OK;
   // argument checks first: they need no device
   if (m < 0 || n < 0 || k < 0 || m > kMaxDim || n > kMaxDim || k > kMaxDim) {
@@ -208,10 +180,6 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     return nullptr;
   }
   if (dtype != GF_F16 && dtype != GF_BF16) {
-    fail(GF_ERR_INVALID_VALUE);
-    return nullptr;
-  }
-  if (epilog < GF_EPILOG_NONE || epilog > GF_EPILOG_DGELU_BGRAD) {
     fail(GF_ERR_INVALID_VALUE);
     return nullptr;
   }
@@ -227,7 +195,7 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     fail(GF_ERR_UNSUPPORTED);
     return nullptr;
   }
-  if (has_bgrad(epilog) && bias_axis != GF_BIAS_COL) {
+  if (has_bgrad(epi) && bias_axis != GF_BIAS_COL) {
     fail(GF_ERR_UNSUPPORTED);
     return nullptr;
   }
@@ -271,7 +239,7 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
   p->n = n;
   p->k = k;
   p->dtype = dtype;
-  p->epilog = epilog;
+  p->epi = epi;
   p->bias_axis = bias_axis;
   p->b_layout = b_layout;
   p->device = dev;
@@ -299,8 +267,8 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     fail(GF_ERR_CUDA);
     return nullptr;
   }
-  if (has_bgrad(epilog) && m > 0 && n > 0) {
-    // sized for the narrowest tile so a later tile option never outgrows it
+  if (has_bgrad(epi) && m > 0 && n > 0) {
+    // one fp32 partial per 128-row block and column, whatever the tile choice
     p->partial_bytes = static_cast<size_t>((m + kBM - 1) / kBM) * static_cast<size_t>(n) * 4;
     if (cudaMalloc(&p->d_partials, p->partial_bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -311,6 +279,191 @@ GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtyp
     }
   }
   return p;
+}
+
+struct ExecArgs {
+  const void* A;
+  const void* B;
+  const void* B2;
+  const void* bias;
+  void* out;
+  const void* aux_in;
+  const void* aux_in2;
+  void* aux_out;
+  void* aux_out2;
+  float* bgrad;
+};
+
+// Checks the pointers the plan's epilog needs, encodes the tensor maps and
+// launches: the execute step of every public entry point.
+gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
+  const bool empty = p->m == 0 || p->n == 0;
+  const int e = p->epi;
+  const bool dual = gf::epi_dual(e);
+  // pointer checks: required pointers present and 16-byte aligned
+  if (!empty) {
+    if (!x.out || !aligned16(x.out)) return fail(GF_ERR_INVALID_VALUE);
+    if (p->k > 0 && (!x.A || !x.B || !aligned16(x.A) || !aligned16(x.B)))
+      return fail(GF_ERR_INVALID_VALUE);
+    if (dual && p->k > 0 && (!x.B2 || !aligned16(x.B2))) return fail(GF_ERR_INVALID_VALUE);
+    if (needs_bias(e) && (!x.bias || !aligned16(x.bias))) return fail(GF_ERR_INVALID_VALUE);
+    if (needs_aux_out(e) && (!x.aux_out || !aligned16(x.aux_out)))
+      return fail(GF_ERR_INVALID_VALUE);
+    if (e == gf::EPI_SWIGLU_SAVE && (!x.aux_out2 || !aligned16(x.aux_out2)))
+      return fail(GF_ERR_INVALID_VALUE);
+    if (needs_aux_in(e) && (!x.aux_in || !aligned16(x.aux_in))) return fail(GF_ERR_INVALID_VALUE);
+    if (e == gf::EPI_DSWIGLU && (!x.aux_in2 || !aligned16(x.aux_in2)))
+      return fail(GF_ERR_INVALID_VALUE);
+  }
+  if (has_bgrad(e) && p->n > 0 && (!x.bgrad || !aligned16(x.bgrad)))
+    return fail(GF_ERR_INVALID_VALUE);
+
+  if (cudaSetDevice(p->device) != cudaSuccess) return fail(GF_ERR_CUDA);
+
+  if (empty) {
+    // nothing to multiply; the bias gradient of zero rows is zero
+    if (has_bgrad(e) && p->n > 0 &&
+        cudaMemsetAsync(x.bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
+    return GF_OK;
+  }
+
+  CUtensorMap tmA, tmB, tmB2;
+  memset(&tmA, 0, sizeof tmA);
+  memset(&tmB, 0, sizeof tmB);
+  memset(&tmB2, 0, sizeof tmB2);
+  if (p->k > 0) {
+    if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
+    // K-major B boxes: a pair CTA loads half of the tile's columns
+    const uint32_t rows_nk = p->pair ? static_cast<uint32_t>(p->tile_n / 2)
+                                     : static_cast<uint32_t>(p->tile_n);
+    const bool ok = p->b_layout == GF_B_KN
+                        ? encode_2d(&tmB, x.B, p->dtype, p->n, p->k, 64, 64)
+                        : encode_2d(&tmB, x.B, p->dtype, p->k, p->n, 64, rows_nk);
+    if (!ok) return fail(GF_ERR_INVALID_VALUE);
+    if (dual && !encode_2d(&tmB2, x.B2, p->dtype, p->k, p->n, 64, rows_nk))
+      return fail(GF_ERR_INVALID_VALUE);
+  }
+
+  gf::GemmParams prm;
+  memset(&prm, 0, sizeof prm);
+  prm.M = static_cast<int32_t>(p->m);
+  prm.N = static_cast<int32_t>(p->n);
+  prm.K = static_cast<int32_t>(p->k);
+  prm.num_m_blocks = p->num_m_blocks;
+  prm.num_n_blocks = p->num_n_blocks;
+  prm.num_k_blocks = p->num_k_blocks;
+  prm.num_tiles = p->num_tiles;
+  prm.group_m = p->group_m;
+  prm.bias_axis = p->bias_axis == GF_BIAS_ROW ? 1 : 0;
+  prm.bias = x.bias;
+  prm.out = x.out;
+  prm.aux_out = static_cast<uint32_t*>(x.aux_out);
+  prm.aux_in = static_cast<const uint32_t*>(x.aux_in);
+  prm.aux_out2 = x.aux_out2;
+  prm.aux_in2 = x.aux_in2;
+  prm.status = p->d_status;
+  prm.wait_limit_ns = p->wait_limit_ns;
+  prm.drop_load = p->drop_load;
+
+  const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
+  if (has_bgrad(e)) {
+    prm.bgrad_atomic = atomic ? 1 : 0;
+    prm.bgrad = atomic ? x.bgrad : p->d_partials;
+    if (atomic && cudaMemsetAsync(x.bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
+  }
+
+  gf::LaunchArgs la;
+  la.tmA = &tmA;
+  la.tmB = &tmB;
+  la.tmB2 = dual ? &tmB2 : &tmB;
+  la.params = &prm;
+  la.grid = p->grid;
+  la.bf16 = p->dtype == GF_BF16 ? 1 : 0;
+  la.b_mn = p->b_layout == GF_B_KN ? 1 : 0;
+  la.tile_n = p->tile_n;
+  la.pair = p->pair;
+  la.stream = st;
+
+  cudaError_t err;
+  switch (e) {
+    case gf::EPI_NONE:
+    case gf::EPI_BIAS: err = gf::launch_none_bias(e, la); break;
+    case gf::EPI_RELU_BIAS:
+    case gf::EPI_RELU_AUX_BIAS: err = gf::launch_relu(e, la); break;
+    case gf::EPI_DRELU_BGRAD: err = gf::launch_drelu(la); break;
+    case gf::EPI_GELU_BIAS:
+    case gf::EPI_GELU_AUX_BIAS:
+    case gf::EPI_DGELU_BGRAD: err = gf::launch_gelu(e, la); break;
+    case gf::EPI_SWIGLU:
+    case gf::EPI_SWIGLU_SAVE:
+    case gf::EPI_DSWIGLU: err = gf::launch_swiglu(e, la); break;
+    default: return fail(GF_ERR_INVALID_VALUE);
+  }
+  if (err != cudaSuccess) return fail(GF_ERR_CUDA);
+  if (has_bgrad(e) && !atomic) {
+    err = gf::launch_bgrad_finalize(p->d_partials, p->num_m_blocks, static_cast<int>(p->n),
+                                    x.bgrad, st);
+    if (err != cudaSuccess) return fail(GF_ERR_CUDA);
+  }
+  return GF_OK;
+}
+
+}  // namespace
+
+namespace gf {
+
+// Shared with the other host entry points of the library (runtime_internal.h).
+gf_status runtime_current_device(int* dev) { return current_device(dev); }
+
+bool runtime_encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner,
+                       uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+  load_driver_entry_points();
+  return g_encode != nullptr && encode_2d(map, ptr, dt, inner, outer, box_inner, box_outer);
+}
+
+}  // namespace gf
+
+extern "C" {
+
+GF_API const char* gf_status_string(gf_status s) {
+  switch (s) {
+    case GF_OK: return "GF_OK";
+    case GF_ERR_INVALID_VALUE: return "GF_ERR_INVALID_VALUE: invalid argument";
+    case GF_ERR_UNSUPPORTED: return "GF_ERR_UNSUPPORTED: valid but not supported";
+    case GF_ERR_NO_DEVICE: return "GF_ERR_NO_DEVICE: no CUDA device";
+    case GF_ERR_CUDA: return "GF_ERR_CUDA: a CUDA call failed";
+    case GF_ERR_OUT_OF_MEMORY: return "GF_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    case GF_ERR_DEVICE_TIMEOUT: return "GF_ERR_DEVICE_TIMEOUT: a bounded wait in a kernel gave up";
+  }
+  return "unknown gf_status";
+}
+
+GF_API gf_status gf_last_error(void) { return g_last; }
+
+GF_API gf_plan* gf_matmul_plan_ex(int64_t m, int64_t n, int64_t k, gf_dtype dtype,
+                                  gf_epilog epilog, gf_bias_axis bias_axis,
+                                  gf_b_layout b_layout) {
+  if (epilog < GF_EPILOG_NONE || epilog > GF_EPILOG_DGELU_BGRAD) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  // the public gf_epilog values are the kernels' epilog codes
+  return plan_create(m, n, k, dtype, static_cast<int>(epilog), bias_axis, b_layout);
+}
+
+GF_API gf_plan* gf_swiglu_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int save_gu) {
+  if (save_gu != 0 && save_gu != 1) {
+    fail(GF_ERR_INVALID_VALUE);
+    return nullptr;
+  }
+  return plan_create(m, n, k, dtype, save_gu ? gf::EPI_SWIGLU_SAVE : gf::EPI_SWIGLU, GF_BIAS_COL,
+                     GF_B_NK);
+}
+
+GF_API gf_plan* gf_dswiglu_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype) {
+  return plan_create(m, n, k, dtype, gf::EPI_DSWIGLU, GF_BIAS_COL, GF_B_KN);
 }
 
 GF_API gf_plan* gf_matmul_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, gf_epilog epilog,
@@ -362,101 +515,25 @@ GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* ti
 GF_API gf_status gf_matmul_execute(const gf_plan* p, const void* A, const void* B,
                                    const void* bias, void* out, const void* aux_in,
                                    void* aux_out, float* bgrad, struct CUstream_st* stream) {
-  if (!p) return fail(GF_ERR_INVALID_VALUE);
-  const bool empty = p->m == 0 || p->n == 0;
-  const gf_epilog e = p->epilog;
-  // pointer checks: required pointers present and 16-byte aligned
-  if (!empty) {
-    if (!out || !aligned16(out)) return fail(GF_ERR_INVALID_VALUE);
-    if (p->k > 0 && (!A || !B || !aligned16(A) || !aligned16(B)))
-      return fail(GF_ERR_INVALID_VALUE);
-    if (needs_bias(e) && (!bias || !aligned16(bias))) return fail(GF_ERR_INVALID_VALUE);
-    if (needs_aux_out(e) && (!aux_out || !aligned16(aux_out)))
-      return fail(GF_ERR_INVALID_VALUE);
-    if (has_bgrad(e) && (!aux_in || !aligned16(aux_in))) return fail(GF_ERR_INVALID_VALUE);
-  }
-  if (has_bgrad(e) && p->n > 0 && (!bgrad || !aligned16(bgrad)))
-    return fail(GF_ERR_INVALID_VALUE);
+  if (!p || p->epi > gf::EPI_DGELU_BGRAD) return fail(GF_ERR_INVALID_VALUE);
+  ExecArgs x = {A, B, nullptr, bias, out, aux_in, nullptr, aux_out, nullptr, bgrad};
+  return execute_impl(p, x, reinterpret_cast<cudaStream_t>(stream));
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaSetDevice(p->device) != cudaSuccess) return fail(GF_ERR_CUDA);
+GF_API gf_status gf_swiglu_execute(const gf_plan* p, const void* x_in, const void* Wg,
+                                   const void* Wu, void* h, void* g_out, void* u_out,
+                                   struct CUstream_st* stream) {
+  if (!p || !gf::epi_dual(p->epi)) return fail(GF_ERR_INVALID_VALUE);
+  ExecArgs x = {x_in, Wg, Wu, nullptr, h, nullptr, nullptr, g_out, u_out, nullptr};
+  return execute_impl(p, x, reinterpret_cast<cudaStream_t>(stream));
+}
 
-  if (empty) {
-    // nothing to multiply; the bias gradient of zero rows is zero
-    if (has_bgrad(e) && p->n > 0 &&
-        cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
-      return fail(GF_ERR_CUDA);
-    return GF_OK;
-  }
-
-  CUtensorMap tmA, tmB;
-  memset(&tmA, 0, sizeof tmA);
-  memset(&tmB, 0, sizeof tmB);
-  if (p->k > 0) {
-    if (!encode_2d(&tmA, A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
-    const bool ok = p->b_layout == GF_B_KN
-                        ? encode_2d(&tmB, B, p->dtype, p->n, p->k, 64, 64)
-                        : encode_2d(&tmB, B, p->dtype, p->k, p->n, 64, p->pair ? 128 : p->tile_n);
-    if (!ok) return fail(GF_ERR_INVALID_VALUE);
-  }
-
-  gf::GemmParams prm;
-  memset(&prm, 0, sizeof prm);
-  prm.M = static_cast<int32_t>(p->m);
-  prm.N = static_cast<int32_t>(p->n);
-  prm.K = static_cast<int32_t>(p->k);
-  prm.num_m_blocks = p->num_m_blocks;
-  prm.num_n_blocks = p->num_n_blocks;
-  prm.num_k_blocks = p->num_k_blocks;
-  prm.num_tiles = p->num_tiles;
-  prm.group_m = p->group_m;
-  prm.bias_axis = p->bias_axis == GF_BIAS_ROW ? 1 : 0;
-  prm.bias = bias;
-  prm.out = out;
-  prm.aux_out = static_cast<uint32_t*>(aux_out);
-  prm.aux_in = static_cast<const uint32_t*>(aux_in);
-  prm.status = p->d_status;
-  prm.wait_limit_ns = p->wait_limit_ns;
-  prm.drop_load = p->drop_load;
-
-  const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
-  if (has_bgrad(e)) {
-    prm.bgrad_atomic = atomic ? 1 : 0;
-    prm.bgrad = atomic ? bgrad : p->d_partials;
-    if (atomic && cudaMemsetAsync(bgrad, 0, static_cast<size_t>(p->n) * 4, st) != cudaSuccess)
-      return fail(GF_ERR_CUDA);
-  }
-
-  gf::LaunchArgs la;
-  la.tmA = &tmA;
-  la.tmB = &tmB;
-  la.params = &prm;
-  la.grid = p->grid;
-  la.bf16 = p->dtype == GF_BF16 ? 1 : 0;
-  la.b_mn = p->b_layout == GF_B_KN ? 1 : 0;
-  la.tile_n = p->tile_n;
-  la.pair = p->pair;
-  la.stream = st;
-
-  cudaError_t err;
-  switch (e) {
-    case GF_EPILOG_NONE: err = gf::launch_none_bias(gf::EPI_NONE, la); break;
-    case GF_EPILOG_BIAS: err = gf::launch_none_bias(gf::EPI_BIAS, la); break;
-    case GF_EPILOG_RELU_BIAS: err = gf::launch_relu(gf::EPI_RELU_BIAS, la); break;
-    case GF_EPILOG_RELU_AUX_BIAS: err = gf::launch_relu(gf::EPI_RELU_AUX_BIAS, la); break;
-    case GF_EPILOG_DRELU_BGRAD: err = gf::launch_drelu(la); break;
-    case GF_EPILOG_GELU_BIAS: err = gf::launch_gelu(gf::EPI_GELU_BIAS, la); break;
-    case GF_EPILOG_GELU_AUX_BIAS: err = gf::launch_gelu(gf::EPI_GELU_AUX_BIAS, la); break;
-    case GF_EPILOG_DGELU_BGRAD: err = gf::launch_gelu(gf::EPI_DGELU_BGRAD, la); break;
-    default: return fail(GF_ERR_INVALID_VALUE);
-  }
-  if (err != cudaSuccess) return fail(GF_ERR_CUDA);
-  if (has_bgrad(e) && !atomic) {
-    err = gf::launch_bgrad_finalize(p->d_partials, p->num_m_blocks, static_cast<int>(p->n), bgrad,
-                                    st);
-    if (err != cudaSuccess) return fail(GF_ERR_CUDA);
-  }
-  return GF_OK;
+GF_API gf_status gf_dswiglu_execute(const gf_plan* p, const void* dout, const void* Wd,
+                                    const void* g, const void* u, void* d_gate, void* d_up,
+                                    struct CUstream_st* stream) {
+  if (!p || p->epi != gf::EPI_DSWIGLU) return fail(GF_ERR_INVALID_VALUE);
+  ExecArgs x = {dout, Wd, nullptr, nullptr, d_gate, g, u, d_up, nullptr, nullptr};
+  return execute_impl(p, x, reinterpret_cast<cudaStream_t>(stream));
 }
 
 GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {

@@ -165,6 +165,48 @@ GF_API gf_status gf_matmul_execute(const gf_plan* plan, const void* A, const voi
                                    void* aux_out, float* bgrad, struct CUstream_st* stream);
 
 /*
+ * Gate+up SwiGLU forward in one kernel ("gemm_swiglu_mlp_fusion.py" sample,
+ * module docstring: silu(x Wg^T) * (x Wu^T) as one fused kernel, the down
+ * projection a separate GEMM). Per output tile the kernel keeps two fp32
+ * accumulators in tensor memory, g = x Wg^T and u = x Wu^T, and its epilogue
+ * writes h = silu(g) * u with silu(g) = g / (1 + e^-g).
+ *
+ * m = rows of x (tokens), n = I (intermediate width), k = H (model width),
+ * same size rules as gf_matmul_plan. save_gu = 1 also stores g and u
+ * (rounded to dtype) for the backward ("save" rather than recompute); 0 does
+ * not. The down projection out = h Wd^T is a plain
+ * gf_matmul_plan_ex(m, H, I, dtype, GF_EPILOG_NONE, GF_BIAS_COL, GF_B_NK).
+ */
+GF_API gf_plan* gf_swiglu_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int save_gu);
+
+/*
+ * x: device [m, k]; Wg, Wu: device [n, k] (nn.Linear weights); h: device
+ * [m, n]; g_out, u_out: device [m, n], required when the plan saves them,
+ * ignored otherwise. All of dtype, 16-byte aligned. Asynchronous on stream,
+ * one kernel launch. Errors as gf_matmul_execute; a plan that is not a
+ * SwiGLU plan gives GF_ERR_INVALID_VALUE.
+ */
+GF_API gf_status gf_swiglu_execute(const gf_plan* plan, const void* x, const void* Wg,
+                                   const void* Wu, void* h, void* g_out, void* u_out,
+                                   struct CUstream_st* stream);
+
+/*
+ * dSwiGLU as the epilogue of dh = dout . Wd ("gemm_swiglu_mlp_fusion.py",
+ * module docstring: the backward's dSwiGLU fused as the epilogue of
+ * matmul(dout, Wd) -> dh). With the saved g and u:
+ *   d_up   = dh * silu(g)
+ *   d_gate = dh * u * sigmoid(g) * (1 + g (1 - sigmoid(g)))
+ * m = rows, n = I, k = H. dout: device [m, k]; Wd: device [k, n] (the
+ * down-projection weight as stored, [H, I]); g, u: device [m, n] from a
+ * saving SwiGLU forward; d_gate, d_up: device [m, n]. All of dtype.
+ */
+GF_API gf_plan* gf_dswiglu_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype);
+
+GF_API gf_status gf_dswiglu_execute(const gf_plan* plan, const void* dout, const void* Wd,
+                                    const void* g, const void* u, void* d_gate, void* d_up,
+                                    struct CUstream_st* stream);
+
+/*
  * Synchronise `stream`, then read and clear the plan's device status word.
  * Returns GF_ERR_DEVICE_TIMEOUT if a bounded wait in a kernel of this plan
  * gave up since the last call (the kernel then skipped the rest of its work
