@@ -299,6 +299,21 @@ def run_gpu(args):
     t_fwd_none, t_fwd_epi = statistics.median(samples["fn"]), statistics.median(samples["fe"])
     t_bwd_none, t_bwd_epi = statistics.median(samples["bn"]), statistics.median(samples["be"])
 
+    # context only: the same two products through torch.matmul (cuBLAS), no epilogue
+    cublas = None
+    if not args.no_cublas:
+        Wt = W.t()
+        c_f = lambda: torch.matmul(X, W, out=Y)  # noqa: E731
+        c_b = lambda: torch.matmul(dY, Wt, out=dZ)  # noqa: E731
+        cf, cb = [], []
+        for _ in range(max(3, min(args.steps, 5))):
+            cf.append(one(c_f))
+            cb.append(one(c_b))
+        cublas = {"fwd_ms": statistics.median(cf), "bwd_ms": statistics.median(cb),
+                  "fwd_tflops": FLOP_PER_GEMM / (statistics.median(cf) * 1e-3) / 1e12,
+                  "bwd_tflops": FLOP_PER_GEMM / (statistics.median(cb) * 1e-3) / 1e12,
+                  "note": "torch.matmul of the same operands, no epilogue; context, not the metric"}
+
     # end to end through the C ABI from pinned host memory
     e2e = None
     if not args.no_e2e:
@@ -377,6 +392,7 @@ def run_gpu(args):
                        "fwd_none": t_fwd_none, "bwd_none": t_bwd_none,
                        "fwd_epi_isolated": t_fwd_epi, "bwd_epi_isolated": t_bwd_epi},
         "epilogue_overhead": {"fwd": t_fwd_epi / t_fwd_none - 1, "bwd": t_bwd_epi / t_bwd_none - 1},
+        "cublas_same_shapes": cublas,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -446,6 +462,7 @@ def main():
     ap.add_argument("--ref-step-rows", type=int, default=4,
                     help="sampled rows per GEMM in each step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gf":
