@@ -10,7 +10,7 @@ namespace gf {
 template <int EPI, typename T, bool B_MN, int BN>
 cudaError_t launch_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_kernel<EPI, T, B_MN, BN>;
-  constexpr int smem = TileCfg<BN, epi_dual(EPI) ? 2 : 1>::kSmemBytes;
+  constexpr int smem = TileCfg<BN, epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kSmemBytes;
   static bool attr_set = false;  // once per instance and process
   if (!attr_set) {
     cudaError_t e =
@@ -25,7 +25,7 @@ cudaError_t launch_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1>::kSmemBytes;
+  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -52,7 +52,7 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN>
 int pair_max_clusters() {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1>::kSmemBytes;
+  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kSmemBytes;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;

@@ -44,21 +44,23 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;  // 64 x 16-bit = 128 bytes = one swizzle row
 constexpr int kThreads = 192;
 
-// NB = number of B operands (2 for the gate+up SwiGLU: two accumulators)
-template <int BN, int NB = 1>
+// NB = number of B operands (2 for the gate+up SwiGLU: two accumulators);
+// RED = the epilog reduces a bias gradient and needs the [4][BN] scratch.
+template <int BN, int NB = 1, bool RED = false>
 struct TileCfg {
   static_assert(BN == 128 || BN == 256, "tile N");
   static_assert(NB == 1 || (NB == 2 && BN == 128), "two B operands need 128-wide tiles");
-  static constexpr int kStages = (BN == 256 || NB == 2) ? 4 : 6;
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;            // one B operand
   static constexpr int kStageBBytes = NB * kBBytes;       // all B operands of a stage
   static constexpr int kAccCols = NB * BN;                // TMEM columns of one accumulator set
   static constexpr int kTmemCols = 2 * kAccCols;          // two accumulator buffers
-  static constexpr int kCtrlBytes = 1024;
-  static constexpr int kRedBytes = 4 * BN * 4;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * (kABytes + kStageBBytes) +
-                                    kCtrlBytes + kRedBytes;
+  static constexpr int kCtrlBytes = kSmemCtrlBytes;
+  static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
+  static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes);
+  static constexpr int kSmemBytes =
+      kSmemAlignSlack + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
+  static_assert(kStages >= 3 && kSmemBytes <= kSmemPerCta, "shared memory budget");
 };
 
 template <typename T>
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = TileCfg<BN, NB>;
+  using C = TileCfg<BN, NB, epi_has_bgrad(EPI)>;
   constexpr int S = C::kStages;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ uint8_t smem_raw[];

@@ -21,20 +21,22 @@
 
 namespace gf {
 
-// NB = number of B operands: 1, or 2 for the gate+up SwiGLU (two accumulators)
-template <int NB = 1>
+// NB = number of B operands: 1, or 2 for the gate+up SwiGLU (two accumulators);
+// RED = the epilog reduces a bias gradient and needs the [4][BN] scratch.
+template <int NB = 1, bool RED = false>
 struct PairCfg {
   static constexpr int BN = NB == 2 ? 128 : 256;       // pair tile 256 x BN per B operand
-  static constexpr int kStages = 6;
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
   static constexpr int kBBytes = (BN / 2) * kBK * 2;   // this CTA's BN/2 columns of one B
   static constexpr int kStageBBytes = NB * kBBytes;    // 16 KB either way
   static constexpr int kAccCols = NB * BN;             // TMEM columns of one accumulator set
   static constexpr int kTmemCols = 2 * kAccCols;       // two accumulator buffers
-  static constexpr int kCtrlBytes = 1024;
-  static constexpr int kRedBytes = 4 * BN * 4;
+  static constexpr int kCtrlBytes = kSmemCtrlBytes;
+  static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
+  static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes);
   static constexpr int kSmemBytes =
-      1024 + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
+      kSmemAlignSlack + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
+  static_assert(kStages >= 3 && kSmemBytes <= kSmemPerCta, "shared memory budget");
 };
 
 // Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = PairCfg<NB>;
+  using C = PairCfg<NB, epi_has_bgrad(EPI)>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;

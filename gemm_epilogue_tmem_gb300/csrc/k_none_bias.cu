@@ -1,4 +1,4 @@
-// Instances: EPILOG_NONE and BIAS.
+// Instances: EPILOG_NONE and BIAS; the ring depth of each kernel shape.
 #include "dispatch.cuh"
 
 namespace gf {
@@ -7,16 +7,16 @@ cudaError_t launch_none_bias(int epi, const LaunchArgs& a) {
   return epi == EPI_BIAS ? launch_epi<EPI_BIAS>(a) : launch_epi<EPI_NONE>(a);
 }
 
-int smem_bytes_for(int tile_n) {
-  return tile_n == 256 ? TileCfg<256>::kSmemBytes : TileCfg<128>::kSmemBytes;
+int stages_for(int tile_n, int pair, int epi) {
+  const bool red = epi_has_bgrad(epi);
+  if (epi_dual(epi))
+    return pair ? (red ? PairCfg<2, true>::kStages : PairCfg<2, false>::kStages)
+                : (red ? TileCfg<128, 2, true>::kStages : TileCfg<128, 2, false>::kStages);
+  if (pair) return red ? PairCfg<1, true>::kStages : PairCfg<1, false>::kStages;
+  if (tile_n == 256) return red ? TileCfg<256, 1, true>::kStages : TileCfg<256, 1, false>::kStages;
+  return red ? TileCfg<128, 1, true>::kStages : TileCfg<128, 1, false>::kStages;
 }
-
-int pair_stages() { return PairCfg<1>::kStages; }
 
 int pair_max_clusters_any() { return pair_max_clusters<EPI_NONE, __half, false>(); }
-
-int stages_for(int tile_n) {
-  return tile_n == 256 ? TileCfg<256>::kStages : TileCfg<128>::kStages;
-}
 
 }  // namespace gf

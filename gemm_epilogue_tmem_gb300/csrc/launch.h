@@ -29,9 +29,8 @@ cudaError_t launch_gelu(int epi, const LaunchArgs& a);        // EPI_GELU_BIAS, 
 cudaError_t launch_swiglu(int epi, const LaunchArgs& a);      // EPI_SWIGLU, _SAVE, EPI_DSWIGLU
 cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
                                   cudaStream_t stream);
-int smem_bytes_for(int tile_n);
-int stages_for(int tile_n);
-int pair_stages();
+// ring depth of the kernel the plan launches
+int stages_for(int tile_n, int pair, int epi);
 // resident CTA pairs of the pair kernel (0 if it cannot launch)
 int pair_max_clusters_any();
 

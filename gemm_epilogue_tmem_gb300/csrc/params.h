@@ -25,6 +25,18 @@ enum Epi : int {
   EPI_DSWIGLU = 10,     // d_gate, d_up of h = silu(g) * u from dh = dout Wd
 };
 
+// Shared-memory budget of one CTA (227 KB) and the ring depth that fills it:
+// 1 KB of alignment slack, 256 B of barriers, the bias-gradient scratch, then
+// as many stages as fit (at most 8).
+constexpr int kSmemPerCta = 227 * 1024;
+constexpr int kSmemAlignSlack = 1024;
+constexpr int kSmemCtrlBytes = 256;
+GF_HD constexpr int ring_stages(int stage_bytes, int red_bytes) {
+  return (kSmemPerCta - kSmemAlignSlack - kSmemCtrlBytes - red_bytes) / stage_bytes > 8
+             ? 8
+             : (kSmemPerCta - kSmemAlignSlack - kSmemCtrlBytes - red_bytes) / stage_bytes;
+}
+
 // epilogs with two B operands (and two accumulators per tile)
 GF_HD constexpr bool epi_dual(int epi) { return epi == EPI_SWIGLU || epi == EPI_SWIGLU_SAVE; }
 

@@ -145,7 +145,7 @@ void plan_tiles(gf_plan* p) {
   p->pair = pair ? 1 : 0;
   if (pair) {
     p->tile_n = pair_n;
-    p->stages = gf::pair_stages();
+    p->stages = gf::stages_for(pair_n, 1, p->epi);
     p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
     const int64_t clusters = pair_tiles < p->max_pair_clusters ? pair_tiles : p->max_pair_clusters;
@@ -162,7 +162,7 @@ void plan_tiles(gf_plan* p) {
     tn = wide >= p->num_sms ? 256 : 128;
   }
   p->tile_n = tn;
-  p->stages = dual ? 4 : gf::stages_for(tn);
+  p->stages = gf::stages_for(tn, 0, p->epi);
   p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
   const int64_t tiles = mblocks * p->num_n_blocks;
   p->num_tiles = static_cast<int>(tiles);
