@@ -433,6 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int loads = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(p.l2_hint_a);
+      const uint64_t pol_b = l2_policy(p.l2_hint_b);
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
@@ -449,15 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (loads != p.drop_load) {
             const uint32_t fb = full0 + 8u * stage;
             mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0);
+            tma_load(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0, p.l2_hint_a, pol_a);
             if (B_MN) {
               for (int j = 0; j < nbox; ++j)
-                tma_load_2d(sB + stage * C::kStageBBytes + j * (64 * kBK * 2), &tmB, fb,
-                            n0 + 64 * j, kb * kBK);
+                tma_load(sB + stage * C::kStageBBytes + j * (64 * kBK * 2), &tmB, fb, n0 + 64 * j,
+                         kb * kBK, p.l2_hint_b, pol_b);
             } else {
-              tma_load_2d(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n0);
+              tma_load(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n0, p.l2_hint_b, pol_b);
               if (NB == 2)  // the second B operand right after the first
-                tma_load_2d(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK, n0);
+                tma_load(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK, n0,
+                         p.l2_hint_b, pol_b);
             }
             issued[stage] = (int)phase;
           }

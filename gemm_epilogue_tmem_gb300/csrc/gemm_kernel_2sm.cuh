@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int loads = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(p.l2_hint_a);
+      const uint64_t pol_b = l2_policy(p.l2_hint_b);
+      const int ha = p.l2_hint_a, hb = p.l2_hint_b;
       for (int t = cluster_id; t < num_pair_tiles && ok; t += num_clusters) {
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
@@ -142,16 +145,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb_local = full0 + 8u * stage;
             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
             if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kStageBBytes));
-            tma_load_2d_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row);
+            tma_load_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row, ha, pol_a);
             if (B_MN) {
-              tma_load_2d_pair(sB + stage * C::kStageBBytes, &tmB, fb, n_col, kb * kBK);
-              tma_load_2d_pair(sB + stage * C::kStageBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
-                               kb * kBK);
+              tma_load_pair(sB + stage * C::kStageBBytes, &tmB, fb, n_col, kb * kBK, hb, pol_b);
+              tma_load_pair(sB + stage * C::kStageBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
+                            kb * kBK, hb, pol_b);
             } else {
-              tma_load_2d_pair(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n_col);
+              tma_load_pair(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n_col, hb, pol_b);
               if (NB == 2)
-                tma_load_2d_pair(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK,
-                                 n_col);
+                tma_load_pair(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK,
+                              n_col, hb, pol_b);
             }
             issued[stage] = (int)phase;
           }

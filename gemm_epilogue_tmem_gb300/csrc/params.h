@@ -72,6 +72,8 @@ struct GemmParams {
   int32_t* status;
   uint64_t wait_limit_ns;
   int32_t drop_load;  // test hook: 1-based index of a stage load to skip (0: none)
+  int32_t l2_hint_a;  // L2 policy of the A loads: 0 none, 1 evict first, 2 evict last
+  int32_t l2_hint_b;  // ... of the B loads
 };
 
 }  // namespace gf

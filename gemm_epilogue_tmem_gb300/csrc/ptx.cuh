@@ -82,6 +82,37 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// L2 eviction-priority policies for cache-hinted TMA loads (createpolicy):
+// 0 = no hint, 1 = evict first (streamed operand), 2 = evict last (operand
+// re-read by the tiles that follow).
+__device__ __forceinline__ uint64_t l2_policy(int kind) {
+  uint64_t pol = 0;
+  if (kind == 1)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else if (kind == 2)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t x, int32_t y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// the loads of the kernels: hinted when the plan asks for an L2 policy
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                         int32_t x, int32_t y, int hint, uint64_t policy) {
+  if (hint)
+    tma_load_2d_hint(dst, map, bar, x, y, policy);
+  else
+    tma_load_2d(dst, map, bar, x, y);
+}
+
 // ------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -266,6 +297,25 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask
 
 __device__ __forceinline__ void sleep_ns(uint32_t ns) {
   asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t cluster_bar, int32_t x, int32_t y,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map,
+                                              uint32_t cluster_bar, int32_t x, int32_t y,
+                                              int hint, uint64_t policy) {
+  if (hint)
+    tma_load_2d_pair_hint(dst, map, cluster_bar, x, y, policy);
+  else
+    tma_load_2d_pair(dst, map, cluster_bar, x, y);
 }
 
 // named barrier over `count` threads (id 0 is __syncthreads)

@@ -33,6 +33,8 @@ struct gf_plan {
   int tile_n;
   int forced_tile_n;
   int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair
+  int forced_group_m;    // 0 auto, else row blocks per raster group
+  int l2_hint_a, l2_hint_b;  // L2 eviction policy of the A / B loads (0 none, 1 first, 2 last)
   int pair;              // the plan uses the CTA-pair kernel
   int max_pair_clusters; // resident CTA pairs (0: the pair kernel cannot run)
   int stages;
@@ -129,7 +131,7 @@ void plan_tiles(gf_plan* p) {
   const int64_t mblocks = (p->m + kBM - 1) / kBM;
   p->num_m_blocks = static_cast<int>(mblocks);
   p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
-  p->group_m = 8;
+  p->group_m = p->forced_group_m > 0 ? p->forced_group_m : 8;
   // The CTA-pair kernel (256 x 256 tiles over two SMs; 256 x 128 per operand
   // with two B operands) moves 2/3 of the operand bytes per flop of the
   // single-CTA tile; take it when its tiles fill the resident pairs, else the
@@ -365,6 +367,8 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.status = p->d_status;
   prm.wait_limit_ns = p->wait_limit_ns;
   prm.drop_load = p->drop_load;
+  prm.l2_hint_a = p->l2_hint_a;
+  prm.l2_hint_b = p->l2_hint_b;
 
   const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
   if (has_bgrad(e)) {
@@ -491,6 +495,17 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
       if (value == 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
       p->forced_kernel = static_cast<int>(value);
+      plan_tiles(p);
+      return GF_OK;
+    case GF_OPT_L2_HINTS:
+      if (value < 0 || value > 22 || value % 10 > 2 || value / 10 > 2)
+        return fail(GF_ERR_INVALID_VALUE);
+      p->l2_hint_a = static_cast<int>(value / 10);
+      p->l2_hint_b = static_cast<int>(value % 10);
+      return GF_OK;
+    case GF_OPT_GROUP_M:
+      if (value < 0 || value > 4096) return fail(GF_ERR_INVALID_VALUE);
+      p->forced_group_m = static_cast<int>(value);
       plan_tiles(p);
       return GF_OK;
     case GF_OPT_FAULT_DROP_LOAD:

@@ -237,8 +237,17 @@ typedef enum gf_option {
   GF_OPT_WAIT_LIMIT_US = 1,
   GF_OPT_TILE_N = 2,
   GF_OPT_FAULT_DROP_LOAD = 3,
-  GF_OPT_KERNEL = 4
+  GF_OPT_KERNEL = 4,
+  GF_OPT_GROUP_M = 5,
+  GF_OPT_L2_HINTS = 6
 } gf_option;
+/* GF_OPT_L2_HINTS: L2 eviction priority of the operand loads, 10 * a + b with
+ * a (for A) and b (for B) each 0 = no hint, 1 = evict first (streamed),
+ * 2 = evict last (re-read by the tiles that follow). */
+/* GF_OPT_GROUP_M: output tiles are visited in groups of this many row blocks
+ * (128 rows, or 256 for the CTA-pair kernel), column by column within a
+ * group, so that concurrently running tiles share operand panels in L2.
+ * 0: the plan's choice (8); 1..4096 otherwise. */
 
 GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);
 
