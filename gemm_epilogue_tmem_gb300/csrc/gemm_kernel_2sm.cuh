@@ -3,17 +3,23 @@
 // tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction); with
 // two B operands (gate+up SwiGLU) a 256 x 128 tile of each, N = 128.
 //
-//   - Each CTA loads its own 128 rows of A and its own 128 columns of B for
-//     every k-slice (TMA, 128-byte swizzle, no multicast): per SM the operand
-//     traffic per flop is 2/3 of the single-CTA 128 x 256 tile's.
+//   - Each CTA loads its own 128 rows of A and its own half of the B columns
+//     for every k-slice (TMA, 128-byte swizzle, no multicast): per SM the
+//     operand traffic per flop is 2/3 of the single-CTA 128 x 256 tile's.
 //   - The stage-full barrier lives in the leader CTA (rank 0): the leader's
 //     producer expects the bytes of both CTAs, the peer's TMA loads signal
 //     the leader's barrier (.cta_group::2).
 //   - The leader's MMA thread issues the pair MMA; commits are multicast to
 //     both CTAs (stage-empty, accumulator-full barriers).
-//   - Each CTA drains its own 128 TMEM lanes (its 128 rows x 256 columns)
+//   - Each CTA drains its own 128 TMEM lanes (its 128 rows x BN columns)
 //     with the same epilogue as the single-CTA kernel; both CTAs' epilogue
 //     warps release the accumulator buffer on the leader's barrier.
+//   - Tiles: static (pair c takes tiles c, c + pairs, ...) or dynamic: the
+//     leader's producer takes the next tile from a global counter and hands
+//     its index to every role of both CTAs through a 4-deep ring in shared
+//     memory. Dynamic keeps the tiles in flight a contiguous run of the
+//     raster order, so operand panels shared by neighbouring tiles are read
+//     from HBM about once instead of once per drifting pair.
 //   - Teardown: drains, then a cluster barrier, then a pair TMEM dealloc.
 #pragma once
 
@@ -37,7 +43,12 @@ struct PairCfg {
   static constexpr int kSmemBytes =
       kSmemAlignSlack + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
   static_assert(kStages >= 3 && kSmemBytes <= kSmemPerCta, "shared memory budget");
+  static_assert(16 * kStages + 128 <= kCtrlBytes, "control region");
 };
+
+constexpr int kTileRing = 4;  // tile indices in flight between the roles (dynamic schedule)
+// consumers of a tile index: leader MMA + 4 epilogue warps, peer producer + 4 epilogue warps
+constexpr int kTileConsumers = 10;
 
 // Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
 __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int& mb2, int& nb) {
@@ -49,6 +60,10 @@ __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int
   const int r = t - group * group_size;
   mb2 = first_m + r % gm;
   nb = r / gm;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 template <int EPI, typename T, bool B_MN>
@@ -77,6 +92,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t done_bar = tempty0 + 16u;  // leader: MMA teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gctrl + 16 * S + 40);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 44);
+  const uint32_t tile_full0 = ctrl + 16u * S + 48u;   // both: kTileRing barriers, index ready
+  const uint32_t tile_empty0 = ctrl + 16u * S + 80u;  // leader: kTileRing barriers, index read
+  const uint32_t ring_s = ctrl + 16u * S + 112u;      // both: kTileRing tile indices
+  volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
 
   const int warp = threadIdx.x >> 5;
@@ -86,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cluster_id = blockIdx.x >> 1;
   const int num_clusters = gridDim.x >> 1;
   const int num_pair_tiles = p.num_tiles;  // the host counts pair tiles for this kernel
+  const bool dynamic = p.tile_counter != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -97,6 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(tempty0, 8);
     mbar_init(tempty0 + 8u, 8);
     mbar_init(done_bar, 1);
+    for (int r = 0; r < kTileRing; ++r) {
+      mbar_init(tile_full0 + 8u * r, 1);
+      mbar_init(tile_empty0 + 8u * r, kTileConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     if (p.num_k_blocks > 0) {
@@ -114,10 +138,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
   bool aborted = false;
+  const uint32_t tile_empty_leader = mapa_shared(tile_empty0, 0);
+
+  // Tile index number `it` of this pair for a consumer role (every role but
+  // the leader's producer): static, or read from the ring and released on
+  // the leader's barrier by lane 0 of the calling warp. -1 ends the loop;
+  // -2 is a wait that gave up.
+  auto consume_tile = [&](int it, bool release) -> int {
+    if (!dynamic) {
+      const int t = cluster_id + it * num_clusters;
+      return t < num_pair_tiles ? t : -1;
+    }
+    const int slot = it % kTileRing;
+    const uint32_t ph = (uint32_t)(it / kTileRing) & 1u;
+    if (!mbar_wait_bounded_cluster(tile_full0 + 8u * slot, ph, abort_flag, p.wait_limit_ns))
+      return -2;
+    const int t = ring[slot];
+    if (release) mbar_arrive_remote(tile_empty_leader + 8u * slot);
+    return t;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && p.num_k_blocks > 0) {
+    if (lane == 0 && (p.num_k_blocks > 0 || dynamic)) {
       int issued[S];
 #pragma unroll
       for (int s = 0; s < S; ++s) issued[s] = -1;
@@ -128,10 +171,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_a = l2_policy(p.l2_hint_a);
       const uint64_t pol_b = l2_policy(p.l2_hint_b);
       const int ha = p.l2_hint_a, hb = p.l2_hint_b;
-      for (int t = cluster_id; t < num_pair_tiles && ok; t += num_clusters) {
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (dynamic && leader) {
+          // take the next tile and hand its index to both CTAs
+          const int slot = it % kTileRing;
+          const uint32_t ph = (uint32_t)(it / kTileRing) & 1u;
+          if (!mbar_wait_bounded_cluster(tile_empty0 + 8u * slot, ph ^ 1u, abort_flag,
+                                         p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
+            aborted = true;
+            break;
+          }
+          t = atomicAdd(p.tile_counter, 1);
+          if (t >= num_pair_tiles) t = -1;
+          ring[slot] = t;
+          st_shared_cluster_u32(mapa_shared(ring_s + 4u * slot, 1), (uint32_t)t);
+          mbar_arrive_remote(mapa_shared(tile_full0 + 8u * slot, 0));
+          mbar_arrive_remote(mapa_shared(tile_full0 + 8u * slot, 1));
+        } else {
+          t = consume_tile(it, true);
+          if (t == -2) {
+            raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
+            aborted = true;
+            break;
+          }
+        }
+        if (t < 0) break;
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
-        const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
+        const int m_row = mb2 * 256 + 128 * (int)rank;     // this CTA's A rows
         const int n_col = nb * BN + (BN / 2) * (int)rank;  // this CTA's B columns
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
@@ -182,8 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int it = 0;
-      for (int t = cluster_id; t < num_pair_tiles && ok; t += num_clusters, ++it) {
+      for (int it = 0; ok; ++it) {
+        const int t = consume_tile(it, true);
+        if (t == -2) {
+          raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
+          aborted = true;
+          break;
+        }
+        if (t < 0) break;
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded_cluster(tempty0 + 8u * buf, use ^ 1u, abort_flag,
@@ -237,11 +312,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int ep_tid = threadIdx.x - 64;
     const uint32_t tempty_leader = mapa_shared(tempty0, 0);
-    int it = 0;
-    for (int t = cluster_id; t < num_pair_tiles; t += num_clusters, ++it) {
+    for (int it = 0;; ++it) {
+      // every lane reads the index; lane 0 releases the slot for the warp
+      int t = consume_tile(it, false);
+      if (dynamic && t != -2) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tile_empty_leader + 8u * (it % kTileRing));
+      }
+      bool ok = t != -2;
+      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
+      if (!ok) {
+        raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+        aborted = true;
+        break;
+      }
+      if (t < 0) break;
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
-      bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
+      ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
       if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
       if (!ok) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);

@@ -30,7 +30,7 @@ enum Epi : int {
 // as many stages as fit (at most 8).
 constexpr int kSmemPerCta = 227 * 1024;
 constexpr int kSmemAlignSlack = 1024;
-constexpr int kSmemCtrlBytes = 256;
+constexpr int kSmemCtrlBytes = 512;
 GF_HD constexpr int ring_stages(int stage_bytes, int red_bytes) {
   return (kSmemPerCta - kSmemAlignSlack - kSmemCtrlBytes - red_bytes) / stage_bytes > 8
              ? 8
@@ -74,6 +74,7 @@ struct GemmParams {
   int32_t drop_load;  // test hook: 1-based index of a stage load to skip (0: none)
   int32_t l2_hint_a;  // L2 policy of the A loads: 0 none, 1 evict first, 2 evict last
   int32_t l2_hint_b;  // ... of the B loads
+  int* tile_counter;  // CTA-pair kernel: global tile counter of the dynamic schedule (null: static)
 };
 
 }  // namespace gf

@@ -35,6 +35,8 @@ struct gf_plan {
   int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair
   int forced_group_m;    // 0 auto, else row blocks per raster group
   int l2_hint_a, l2_hint_b;  // L2 eviction policy of the A / B loads (0 none, 1 first, 2 last)
+  int one_tile_per_cta;  // 1: grid of one tile per CTA (pair); the hardware orders the tiles
+  int dynamic_schedule;  // 1: persistent CTA pairs take tiles from a global counter
   int pair;              // the plan uses the CTA-pair kernel
   int max_pair_clusters; // resident CTA pairs (0: the pair kernel cannot run)
   int stages;
@@ -151,7 +153,7 @@ void plan_tiles(gf_plan* p) {
     p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
     const int64_t clusters = pair_tiles < p->max_pair_clusters ? pair_tiles : p->max_pair_clusters;
-    p->grid = static_cast<int>(2 * clusters);
+    p->grid = static_cast<int>(2 * (p->one_tile_per_cta ? pair_tiles : clusters));
     return;
   }
   int tn = p->forced_tile_n;
@@ -168,7 +170,7 @@ void plan_tiles(gf_plan* p) {
   p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
   const int64_t tiles = mblocks * p->num_n_blocks;
   p->num_tiles = static_cast<int>(tiles);
-  p->grid = static_cast<int>(tiles < p->num_sms ? tiles : p->num_sms);
+  p->grid = static_cast<int>(p->one_tile_per_cta || tiles < p->num_sms ? tiles : p->num_sms);
 }
 
 // Validation, device checks, tile choice and workspace: the plan step of
@@ -369,6 +371,12 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.drop_load = p->drop_load;
   prm.l2_hint_a = p->l2_hint_a;
   prm.l2_hint_b = p->l2_hint_b;
+  if (p->pair && p->dynamic_schedule && !p->one_tile_per_cta) {
+    // the tile counter sits in the plan's status block, 64 bytes past the status word
+    prm.tile_counter = p->d_status + 16;
+    if (cudaMemsetAsync(prm.tile_counter, 0, sizeof(int), st) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
+  }
 
   const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
   if (has_bgrad(e)) {
@@ -502,6 +510,12 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
         return fail(GF_ERR_INVALID_VALUE);
       p->l2_hint_a = static_cast<int>(value / 10);
       p->l2_hint_b = static_cast<int>(value % 10);
+      return GF_OK;
+    case GF_OPT_SCHEDULE:
+      if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
+      p->one_tile_per_cta = value == 1 ? 1 : 0;
+      p->dynamic_schedule = value == 2 ? 1 : 0;
+      plan_tiles(p);
       return GF_OK;
     case GF_OPT_GROUP_M:
       if (value < 0 || value > 4096) return fail(GF_ERR_INVALID_VALUE);

@@ -239,8 +239,15 @@ typedef enum gf_option {
   GF_OPT_FAULT_DROP_LOAD = 3,
   GF_OPT_KERNEL = 4,
   GF_OPT_GROUP_M = 5,
-  GF_OPT_L2_HINTS = 6
+  GF_OPT_L2_HINTS = 6,
+  GF_OPT_SCHEDULE = 7
 } gf_option;
+/* GF_OPT_SCHEDULE: 0 persistent, static (one CTA or CTA pair per SM walks
+ * every gridDim-th tile and overlaps each epilogue with the next tile's
+ * mainloop); 1 one tile per CTA (pair), launched in raster order by the
+ * hardware scheduler; 2 persistent, dynamic (CTA-pair kernel: each pair takes
+ * the next tile from a counter, so the tiles in flight stay a contiguous run
+ * of the raster order; the counter lives in the plan's workspace). */
 /* GF_OPT_L2_HINTS: L2 eviction priority of the operand loads, 10 * a + b with
  * a (for A) and b (for B) each 0 = no hint, 1 = evict first (streamed),
  * 2 = evict last (re-read by the tiles that follow). */

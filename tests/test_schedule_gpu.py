@@ -1,0 +1,109 @@
+"""Tile schedules of the persistent kernels (static, one tile per CTA pair,
+dynamic counter) and raster groups give the oracle's results; the dynamic
+schedule also keeps its bounded waits (a skipped load is reported, and the
+next call is correct)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import BGRAD_NMAX, BGRAD_REL, assert_close, mask_mismatch, to_dev, to_host_f32, \
+    to_host_words, unpack_words
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import gemm_epilogue_tmem_gb300 as gf  # noqa: E402
+
+M, N, K = 3000, 2568, 264
+
+
+@pytest.fixture(scope="module")
+def data():
+    X = synth.normal((M, K), synth.F16, 31, synth.TID_A, 1.0)
+    W = synth.normal((K, N), synth.F16, 31, synth.TID_B, 1 / np.sqrt(K))
+    Wt = synth.normal((N, K), synth.F16, 31, synth.TID_W2, 1 / np.sqrt(K))
+    b = synth.normal((N,), synth.F16, 31, synth.TID_BIAS, 0.1)
+    words = synth.mask_words(M, N, 31)
+    y_o, z_o = oracle.relu_bias(X, W, b, oracle.F16)
+    dz_o, bgrad_o, _ = oracle.drelu_bgrad(X, Wt, words, oracle.F16, oracle.B_NK)
+    return X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o
+
+
+@pytest.mark.parametrize("schedule", [0, 1, 2])
+@pytest.mark.parametrize("group_m", [1, 4, 8])
+def test_forward_schedules(data, schedule, group_m):
+    X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    aux = torch.empty(((M + 31) // 32, N), dtype=torch.int32, device="cuda")
+    plan = gf.gf_matmul_plan(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, schedule)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_GROUP_M, group_m)
+    for _ in range(2):  # the dynamic counter is reset for every call
+        gf.gf_matmul_execute(plan, to_dev(X, 0), to_dev(W, 0), bias=to_dev(b, 0), out=out,
+                             aux_out=aux)
+        assert gf.gf_plan_status(plan) == gf.GF_OK
+        assert_close(to_host_f32(out), oracle.decode(y_o, 0), what="Y")
+        outside, _ = mask_mismatch(unpack_words(to_host_words(aux), M), z_o)
+        assert outside == 0
+        out.zero_()
+    plan.free()
+
+
+@pytest.mark.parametrize("schedule", [0, 2])
+@pytest.mark.parametrize("mode", [gf.GF_BGRAD_TWO_PASS, gf.GF_BGRAD_ATOMIC])
+def test_backward_schedules(data, schedule, mode):
+    X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    bgrad = torch.empty((N,), dtype=torch.float32, device="cuda")
+    plan = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                gf.GF_B_NK)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, schedule)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_BGRAD_MODE, mode)
+    gf.gf_matmul_execute(plan, to_dev(X, 0), to_dev(Wt, 0), out=out, aux_in=to_dev(words, 0),
+                         bgrad=bgrad)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    assert_close(to_host_f32(out), oracle.decode(dz_o, 0), what="dZ")
+    assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
+
+
+def test_dynamic_schedule_swiglu_and_gelu():
+    Mh, I, H = 1536, 1032, 256
+    d = synth.BF16
+    x = synth.normal((Mh, H), d, 32, synth.TID_A, 1.0)
+    Wg = synth.normal((I, H), d, 32, synth.TID_WG, 0.1)
+    Wu = synth.normal((I, H), d, 32, synth.TID_WU, 0.1)
+    h = torch.empty((Mh, I), dtype=torch.bfloat16, device="cuda")
+    plan = gf.gf_swiglu_plan(Mh, I, H, d)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, 2)
+    gf.gf_swiglu_execute(plan, to_dev(x, d), to_dev(Wg, d), to_dev(Wu, d), h)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    h_o = oracle.swiglu_forward(x, Wg, Wu, d)[0]
+    assert_close(to_host_f32(h), oracle.decode(h_o, d), what="h")
+
+
+def test_dynamic_schedule_wait_limit():
+    X = torch.randn((1024, 512), device="cuda").half()
+    W = torch.randn((512, 1024), device="cuda").half() / 16
+    bias = torch.zeros(1024, device="cuda").half()
+    out = torch.empty((1024, 1024), dtype=torch.float16, device="cuda")
+    plan = gf.gf_matmul_plan(1024, 1024, 512, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_WAIT_LIMIT_US, 20000)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 3)
+    gf.gf_matmul_execute(plan, X, W, bias=bias, out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_ERR_DEVICE_TIMEOUT
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 0)
+    gf.gf_matmul_execute(plan, X, W, bias=bias, out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    ref = torch.relu(X.float() @ W.float())
+    assert float((out.float() - ref).abs().max() / ref.abs().max()) < 2e-2
+    plan.free()
