@@ -36,7 +36,7 @@ struct gf_plan {
   int forced_group_m;    // 0 auto, else row blocks per raster group
   int l2_hint_a, l2_hint_b;  // L2 eviction policy of the A / B loads (0 none, 1 first, 2 last)
   int one_tile_per_cta;  // 1: grid of one tile per CTA (pair); the hardware orders the tiles
-  int dynamic_schedule;  // 1: persistent CTA pairs take tiles from a global counter
+  int static_schedule;   // 1: persistent CTA pairs walk every gridDim-th tile (default: counter)
   int pair;              // the plan uses the CTA-pair kernel
   int max_pair_clusters; // resident CTA pairs (0: the pair kernel cannot run)
   int stages;
@@ -371,7 +371,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.drop_load = p->drop_load;
   prm.l2_hint_a = p->l2_hint_a;
   prm.l2_hint_b = p->l2_hint_b;
-  if (p->pair && p->dynamic_schedule && !p->one_tile_per_cta) {
+  if (p->pair && !p->static_schedule && !p->one_tile_per_cta) {
     // the tile counter sits in the plan's status block, 64 bytes past the status word
     prm.tile_counter = p->d_status + 16;
     if (cudaMemsetAsync(prm.tile_counter, 0, sizeof(int), st) != cudaSuccess)
@@ -512,9 +512,9 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       p->l2_hint_b = static_cast<int>(value % 10);
       return GF_OK;
     case GF_OPT_SCHEDULE:
-      if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
+      if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
       p->one_tile_per_cta = value == 1 ? 1 : 0;
-      p->dynamic_schedule = value == 2 ? 1 : 0;
+      p->static_schedule = value == 3 ? 1 : 0;
       plan_tiles(p);
       return GF_OK;
     case GF_OPT_GROUP_M:

@@ -242,12 +242,14 @@ typedef enum gf_option {
   GF_OPT_L2_HINTS = 6,
   GF_OPT_SCHEDULE = 7
 } gf_option;
-/* GF_OPT_SCHEDULE: 0 persistent, static (one CTA or CTA pair per SM walks
- * every gridDim-th tile and overlaps each epilogue with the next tile's
- * mainloop); 1 one tile per CTA (pair), launched in raster order by the
- * hardware scheduler; 2 persistent, dynamic (CTA-pair kernel: each pair takes
- * the next tile from a counter, so the tiles in flight stay a contiguous run
- * of the raster order; the counter lives in the plan's workspace). */
+/* GF_OPT_SCHEDULE: how persistent CTAs (or CTA pairs) walk the output tiles,
+ * overlapping each tile's epilogue with the next tile's mainloop.
+ *   0 the plan's choice: 2 for the CTA-pair kernel, 3 for the single-CTA one;
+ *   1 one tile per CTA (pair), launched in raster order by the hardware;
+ *   2 dynamic (CTA-pair kernel): each pair takes the next tile from a counter
+ *     in the plan's workspace, so the tiles in flight stay a contiguous run of
+ *     the raster order and share their operand panels in L2;
+ *   3 static: pair (CTA) c takes tiles c, c + grid, c + 2 grid, ... */
 /* GF_OPT_L2_HINTS: L2 eviction priority of the operand loads, 10 * a + b with
  * a (for A) and b (for B) each 0 = no hint, 1 = evict first (streamed),
  * 2 = evict last (re-read by the tiles that follow). */

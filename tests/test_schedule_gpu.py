@@ -32,7 +32,7 @@ def data():
     return X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3])
 @pytest.mark.parametrize("group_m", [1, 4, 8])
 def test_forward_schedules(data, schedule, group_m):
     X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
@@ -53,7 +53,7 @@ def test_forward_schedules(data, schedule, group_m):
     plan.free()
 
 
-@pytest.mark.parametrize("schedule", [0, 2])
+@pytest.mark.parametrize("schedule", [0, 3])
 @pytest.mark.parametrize("mode", [gf.GF_BGRAD_TWO_PASS, gf.GF_BGRAD_ATOMIC])
 def test_backward_schedules(data, schedule, mode):
     X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
