@@ -41,6 +41,44 @@ FLOP_PER_GEMM = 2.0 * M * N * K
 FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
+                               "linear_pair_fp16_65536x16384x8192_dram_traffic.md")
+
+
+def kernel_sources_sha256() -> str:
+    """Digest of the kernel sources: a recorded ncu traffic figure is only
+    reported while the kernels it was measured on are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gemm_epilogue_tmem_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """(fwd, bwd) DRAM bytes per launch from the committed ncu summary, or
+    None when it is missing or was taken on other kernel sources."""
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_PROFILE) as f:
+        for line in f:
+            line = line.strip().strip("`")
+            if ":" in line and line.split(":")[0] in ("sources_sha256", "fwd_bytes_per_launch",
+                                                      "bwd_bytes_per_launch"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("sources_sha256") != kernel_sources_sha256():
+        return None
+    try:
+        return float(vals["fwd_bytes_per_launch"]), float(vals["bwd_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -48,6 +86,16 @@ def peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK), "fallback"
+
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over the ranks of the default process group (the
+    slowest replica's time bounds the job)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def dist_env():
@@ -335,10 +383,7 @@ def run_gpu(args):
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+        ms_total = max_over_ranks(ms_total, dev)
 
     # epilogue overhead: the same kernels and tiles with no epilogue
     # interleaved, so that clock and power drift hit both variants alike
@@ -398,6 +443,8 @@ def run_gpu(args):
     ms_step = ms_total / args.steps
     value = world * 2 * FLOP_PER_GEMM / (ms_step * 1e-3) / 1e12
     fwd_avg, bwd_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    rec = recorded_traffic()
+    traffic = None if rec is None else (rec[0] if fwd_avg >= bwd_avg else rec[1])
     dom_name, dom_ms = ("fused forward RELU_AUX_BIAS", fwd_avg) if fwd_avg >= bwd_avg else \
         ("fused backward DRELU_BGRAD (+ finalize)", bwd_avg)
     peak_key = "bf16_tflops_sustained" if "bf16_tflops_sustained" in pk else "bf16_tflops"
@@ -423,7 +470,7 @@ def run_gpu(args):
                         "peak_kind": f"{pk_kind} {peak_key}",
                         "vs_nominal_2250": 100 * value / world / 2250.0},
         "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{pk_kind} {peak_key}",
                      "algorithmic_flop_per_launch": FLOP_PER_GEMM},
         "kernels_ms": {"fwd_relu_aux_bias": fwd_avg, "bwd_drelu_bgrad": bwd_avg,
@@ -484,8 +531,78 @@ def run_profile_case(args):
     return 0 if st == gf.GF_OK else 1
 
 
+def run_compare_schedules(args):
+    """Steady-state comparison of the CTA-pair kernel's tile schedules on the
+    full-size fused forward, and torch.matmul (cuBLAS, no epilogue) for
+    context: each configuration runs `--seconds` back to back after a
+    warm-up while nvidia-smi samples SM clock and power; the list is run
+    twice. One JSON line per run."""
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+
+    gf.build()
+    synth.build_cuda()
+    sp = torch.cuda.current_stream().cuda_stream
+    X = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    W = torch.empty((K, N), dtype=torch.float16, device="cuda")
+    bias = torch.empty((N,), dtype=torch.float16, device="cuda")
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    aux = torch.empty((M // 32, N), dtype=torch.int32, device="cuda")
+    synth.dev_normal(X, synth.F16, 0, synth.TID_A, 1.0, sp)
+    synth.dev_normal(W, synth.F16, 0, synth.TID_B, 1 / 128, sp)
+    synth.dev_normal(bias, synth.F16, 0, synth.TID_BIAS, 0.1, sp)
+    torch.cuda.synchronize()
+    cfgs = {}
+    for name, sched in (("dynamic", 2), ("static", 3), ("one_tile_per_pair", 1)):
+        plan = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL,
+                                    gf.GF_B_KN)
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+        gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, sched)
+        cfgs[name] = (plan, (lambda p: lambda: gf.gf_matmul_execute(
+            p, X, W, bias=bias, out=Y, aux_out=aux, stream=sp))(plan))
+    cfgs["cublas_matmul_no_epilogue"] = (None, lambda: torch.matmul(X, W, out=Y))
+
+    def run(fn):
+        sampler = ClockSampler(0)
+        sampler.start()
+        t_end = time.time() + 1.5
+        while time.time() < t_end:
+            fn()
+            torch.cuda.synchronize()
+        n0 = len(sampler.lines)
+        times = []
+        t_end = time.time() + args.seconds
+        while time.time() < t_end:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        sampler.lines = sampler.lines[n0:]
+        clk = sampler.stop()
+        ms = statistics.median(times)
+        return {"ms": ms, "tflops": FLOP_PER_GEMM / (ms * 1e-3) / 1e12, "sm_mhz": clk["sm_mhz"],
+                "power_w": clk.get("power_w_median"), "launches": len(times),
+                "gcycles": ms * 1e-3 * clk["sm_mhz"] * 1e6 / 1e9 if clk["sm_mhz"] else None}
+
+    for rnd in range(2):
+        for name, (plan, fn) in cfgs.items():
+            print(json.dumps({"config": name, "round": rnd, "shape": [M, N, K], **run(fn)}),
+                  flush=True)
+    for plan, _ in cfgs.values():
+        if plan is not None:
+            plan.free()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--compare-schedules", action="store_true",
+                    help="steady-state comparison of the tile schedules (not the bench line)")
+    ap.add_argument("--seconds", type=float, default=4.0)
     ap.add_argument("--profile-case", default="",
                     help="M,N,K: run one fused GEMM of this shape (for ncu captures)")
     ap.add_argument("--epilog", default="relu_aux_bias",
@@ -509,6 +626,8 @@ def main():
         return run_reference(args)
     if args.profile_case:
         return run_profile_case(args)
+    if args.compare_schedules:
+        return run_compare_schedules(args)
     return run_gpu(args)
 
 
