@@ -343,6 +343,11 @@ def run_gpu(args):
     bwd_none = gf.gf_matmul_plan_ex(M, K, N, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
                                     gf.GF_B_NK)
     launches_per_step = 3  # fused forward, fused backward, bgrad finalize
+    if args.autotune:
+        gf.gf_matmul_autotune(fwd, X, W, bias=bias, out=Y, aux_out=aux, stream=sp, reps=2)
+        gf.gf_matmul_autotune(bwd, dY, W, out=dZ, aux_in=mask, bgrad=bgrad, stream=sp, reps=2)
+    plans = {"fwd": gf.gf_plan_describe(fwd), "bwd": gf.gf_plan_describe(bwd),
+             "autotuned": bool(args.autotune)}
 
     def step(ev=None):
         if ev is not None:
@@ -384,6 +389,35 @@ def run_gpu(args):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
     if world > 1:
         ms_total = max_over_ranks(ms_total, dev)
+
+    # the same step captured once in a CUDA graph and replayed
+    graph = None
+    if not args.no_graph:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                cs = torch.cuda.current_stream().cuda_stream
+                gf.gf_matmul_execute(fwd, X, W, bias=bias, out=Y, aux_out=aux, stream=cs)
+                gf.gf_matmul_execute(bwd, dY, W, out=dZ, aux_in=mask, bgrad=bgrad, stream=cs)
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(args.steps, 20))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        gms = a.elapsed_time(b) / reps
+        graph = {"ms_per_step": gms, "value": 2 * FLOP_PER_GEMM / (gms * 1e-3) / 1e12,
+                 "unit": "TFLOP/s", "replays": reps,
+                 "status_ok": gf.gf_plan_status(fwd, sp) == gf.GF_OK and
+                 gf.gf_plan_status(bwd, sp) == gf.GF_OK}
+        del g
 
     # epilogue overhead: the same kernels and tiles with no epilogue
     # interleaved, so that clock and power drift hit both variants alike
@@ -465,7 +499,7 @@ def run_gpu(args):
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "seed": 0,
                    "l2": "inputs larger than L2 (X 2.1 GB, dY 1.1 GB); no flush",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU", "plans": plans},
         "pct_of_peak": {"value": 100 * value / world / peak, "peak_tflops": peak,
                         "peak_kind": f"{pk_kind} {peak_key}",
                         "vs_nominal_2250": 100 * value / world / 2250.0},
@@ -478,6 +512,7 @@ def run_gpu(args):
                        "fwd_epi_isolated": t_fwd_epi, "bwd_epi_isolated": t_bwd_epi},
         "epilogue_overhead": {"fwd": t_fwd_epi / t_fwd_none - 1, "bwd": t_bwd_epi / t_bwd_none - 1},
         "cublas_same_shapes": cublas,
+        "cuda_graph_replay": graph,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -618,6 +653,9 @@ def main():
                     help="sampled rows per GEMM in each step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--autotune", action="store_true",
+                    help="let gf_matmul_autotune pick the kernels before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gf":

@@ -97,6 +97,8 @@ def lib(path: str | None = None):
         L.gf_dswiglu_plan.argtypes = [_I64, _I64, _I64, _I32]
         L.gf_dswiglu_execute.restype = _I32
         L.gf_dswiglu_execute.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
+        L.gf_matmul_autotune.restype = _I32
+        L.gf_matmul_autotune.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I32]
         L.gf_drelu_bgrad_noalloc.restype = _I32
         L.gf_drelu_bgrad_noalloc.argtypes = [_I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]
         _lib = L
@@ -173,6 +175,17 @@ def gf_matmul_execute(plan: Plan, A, B, bias=None, out=None, aux_in=None, aux_ou
                                  _ptr(aux_in), _ptr(aux_out), _ptr(bgrad), _stream(stream))
     if rc != GF_OK:
         raise GfError(rc, "gf_matmul_execute")
+
+
+def gf_matmul_autotune(plan: Plan, A, B, bias=None, out=None, aux_in=None, aux_out=None,
+                       bgrad=None, stream=None, reps: int = 3) -> dict:
+    """Time the library's kernel/tile/schedule candidates on these buffers,
+    keep the fastest in the plan and return its description."""
+    rc = lib().gf_matmul_autotune(plan.handle, _ptr(A), _ptr(B), _ptr(bias), _ptr(out),
+                                  _ptr(aux_in), _ptr(aux_out), _ptr(bgrad), _stream(stream), reps)
+    if rc != GF_OK:
+        raise GfError(rc, "gf_matmul_autotune")
+    return gf_plan_describe(plan)
 
 
 def gf_swiglu_plan(m: int, n: int, k: int, dtype: int, save_gu: bool = False) -> Plan:

@@ -530,6 +530,73 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
   return fail(GF_ERR_INVALID_VALUE);
 }
 
+GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, const void* bias,
+                                    void* out, const void* aux_in, void* aux_out, float* bgrad,
+                                    struct CUstream_st* stream, int32_t reps) {
+  if (!p || p->epi > gf::EPI_DGELU_BGRAD || reps < 1 || reps > 100)
+    return fail(GF_ERR_INVALID_VALUE);
+  if (p->m == 0 || p->n == 0) return GF_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  ExecArgs x = {A, B, nullptr, bias, out, aux_in, nullptr, aux_out, nullptr, bgrad};
+  // candidates: {kernel (1 single, 2 pair), tile_n, schedule, group_m}
+  struct Cand { int kernel, tile_n, schedule, group_m; };
+  const Cand cands[] = {{2, 0, 2, 8}, {2, 0, 2, 4}, {2, 0, 2, 16}, {2, 0, 3, 8},
+                        {1, 256, 0, 8}, {1, 128, 0, 8}, {1, 256, 0, 4}};
+  const int saved[5] = {p->forced_kernel, p->forced_tile_n, p->one_tile_per_cta,
+                        p->static_schedule, p->forced_group_m};
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+    return fail(GF_ERR_CUDA);
+  float best_ms = -1.f;
+  Cand best = cands[0];
+  gf_status st_out = GF_OK;
+  for (const Cand& c : cands) {
+    if (c.kernel == 2 && p->max_pair_clusters == 0) continue;
+    p->forced_kernel = c.kernel;
+    p->forced_tile_n = c.tile_n;
+    p->one_tile_per_cta = 0;
+    p->static_schedule = c.schedule == 3 ? 1 : 0;
+    p->forced_group_m = c.group_m;
+    plan_tiles(p);
+    gf_status s = execute_impl(p, x, st);  // warm-up, and the check of the arguments
+    if (s != GF_OK) {
+      st_out = s;
+      break;
+    }
+    cudaEventRecord(e0, st);
+    for (int r = 0; r < reps && s == GF_OK; ++r) s = execute_impl(p, x, st);
+    cudaEventRecord(e1, st);
+    if (s != GF_OK || cudaEventSynchronize(e1) != cudaSuccess) {
+      st_out = s != GF_OK ? s : GF_ERR_CUDA;
+      break;
+    }
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    if (best_ms < 0.f || ms < best_ms) {
+      best_ms = ms;
+      best = c;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st_out != GF_OK || best_ms < 0.f) {
+    p->forced_kernel = saved[0];
+    p->forced_tile_n = saved[1];
+    p->one_tile_per_cta = saved[2];
+    p->static_schedule = saved[3];
+    p->forced_group_m = saved[4];
+    plan_tiles(p);
+    return st_out != GF_OK ? fail(st_out) : fail(GF_ERR_UNSUPPORTED);
+  }
+  p->forced_kernel = best.kernel;
+  p->forced_tile_n = best.tile_n;
+  p->one_tile_per_cta = 0;
+  p->static_schedule = best.schedule == 3 ? 1 : 0;
+  p->forced_group_m = best.group_m;
+  plan_tiles(p);
+  return GF_OK;
+}
+
 GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* tile_n,
                                   int32_t* stages, int32_t* grid, int64_t* workspace_bytes) {
   if (!p) return fail(GF_ERR_INVALID_VALUE);

@@ -260,6 +260,22 @@ typedef enum gf_option {
 
 GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);
 
+/*
+ * Plan-time autotuning of a gf_matmul plan (the plan-time algorithm search of
+ * the nvmath-python / cuBLASLt page, "limitations" paragraph: autotuning
+ * through MatmulPlanPreferences; here a search over this library's own
+ * kernels). Runs the planned product once per candidate (CTA-pair kernel
+ * with dynamic or static schedule and raster groups of 4, 8 or 16 tile rows;
+ * single-CTA kernel with 256- or 128-wide tiles) on the caller's buffers,
+ * `reps` timed launches each after one warm-up, synchronising `stream`, and
+ * keeps the fastest in the plan. The outputs hold the result of the last
+ * launch. Arguments as gf_matmul_execute; reps in 1..100.
+ */
+GF_API gf_status gf_matmul_autotune(gf_plan* plan, const void* A, const void* B,
+                                    const void* bias, void* out, const void* aux_in,
+                                    void* aux_out, float* bgrad, struct CUstream_st* stream,
+                                    int32_t reps);
+
 /* Read back the plan's choices: tile_m, tile_n, stages, grid size (CTAs per
  * launch), workspace bytes. Any out-pointer may be NULL. */
 GF_API gf_status gf_plan_describe(const gf_plan* plan, int32_t* tile_m, int32_t* tile_n,

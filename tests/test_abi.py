@@ -64,6 +64,8 @@ def test_null_plan_calls(L):
         gf.GF_ERR_INVALID_VALUE
     assert L.gf_plan_status(None, None) == gf.GF_ERR_INVALID_VALUE
     assert L.gf_plan_set_option(None, 0, 0) == gf.GF_ERR_INVALID_VALUE
+    assert L.gf_matmul_autotune(None, None, None, None, None, None, None, None, None, 3) == \
+        gf.GF_ERR_INVALID_VALUE
     L.gf_plan_free(None)
 
 

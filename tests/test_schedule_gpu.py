@@ -107,3 +107,46 @@ def test_dynamic_schedule_wait_limit():
     ref = torch.relu(X.float() @ W.float())
     assert float((out.float() - ref).abs().max() / ref.abs().max()) < 2e-2
     plan.free()
+
+
+@pytest.mark.parametrize("epilog", ["fwd", "bwd"])
+def test_autotune_keeps_a_correct_choice(data, epilog):
+    """The autotuned plan still gives the oracle's results, and its
+    description is one of the candidate configurations."""
+    X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    if epilog == "fwd":
+        aux = torch.empty(((M + 31) // 32, N), dtype=torch.int32, device="cuda")
+        plan = gf.gf_matmul_plan(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+        args = dict(A=to_dev(X, 0), B=to_dev(W, 0), bias=to_dev(b, 0), out=out, aux_out=aux)
+    else:
+        bgrad = torch.empty((N,), dtype=torch.float32, device="cuda")
+        plan = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                    gf.GF_B_NK)
+        args = dict(A=to_dev(X, 0), B=to_dev(Wt, 0), out=out, aux_in=to_dev(words, 0),
+                    bgrad=bgrad)
+    desc = gf.gf_matmul_autotune(plan, reps=2, **args)
+    assert (desc["tile_m"], desc["tile_n"]) in ((256, 256), (128, 256), (128, 128))
+    out.zero_()
+    gf.gf_matmul_execute(plan, **args)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    assert gf.gf_plan_describe(plan) == desc
+    plan.free()
+    if epilog == "fwd":
+        assert_close(to_host_f32(out), oracle.decode(y_o, 0), what="Y")
+        outside, _ = mask_mismatch(unpack_words(to_host_words(aux), M), z_o)
+        assert outside == 0
+    else:
+        assert_close(to_host_f32(out), oracle.decode(dz_o, 0), what="dZ")
+        assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
+
+
+def test_autotune_rejects_bad_reps():
+    plan = gf.gf_matmul_plan(256, 256, 64, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL)
+    a = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
+    w = torch.zeros((64, 256), dtype=torch.float16, device="cuda")
+    o = torch.empty((256, 256), dtype=torch.float16, device="cuda")
+    for reps in (0, 101):
+        with pytest.raises(gf.GfError):
+            gf.gf_matmul_autotune(plan, a, w, out=o, reps=reps)
+    plan.free()
