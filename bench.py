@@ -566,6 +566,218 @@ def run_profile_case(args):
     return 0 if st == gf.GF_OK else 1
 
 
+def _interleaved(torch, fns: dict, reps: int, rounds: int = 3) -> dict:
+    """Median ms per call of each function: `reps` back-to-back calls between
+    two events on the current stream, the functions taken in turn `rounds`
+    times so that clock and power drift fall on all of them alike."""
+    for fn in fns.values():
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    times = {k: [] for k in fns}
+    s = torch.cuda.current_stream()
+    for _ in range(rounds):
+        for name, fn in fns.items():
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            for _ in range(reps):
+                fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            times[name].append(a.elapsed_time(b) / reps)
+    return {k: statistics.median(v) for k, v in times.items()}
+
+
+def _dev_fill(torch, recipe, name, dev, sp, view=None):
+    t = recipe.tensors[name]
+    tdt = torch.float16 if recipe.dtype == synth.F16 else torch.bfloat16
+    x = view if view is not None else torch.empty(t.shape, dtype=tdt, device=dev)
+    synth.dev_normal(x, recipe.dtype, 0, t.tensor_id, t.sigma, sp)
+    return x
+
+
+def run_gelu_workload(args, gf, torch, dev, sp, peak, pk):
+    """GELU_AUX_BIAS forward X[8192,4096] W[4096,16384] + DGELU_BGRAD backward
+    dY[8192,16384] W^T on a seeded pre-activation [8192,4096], bf16."""
+    import torch.nn.functional as F
+    rc = synth.GELU_BIAS
+    Mg, Kg = rc.tensors["X"].shape
+    Ng = rc.tensors["W"].shape[1]
+    bf = torch.bfloat16
+    X, W, bias, dY, pre_b = (_dev_fill(torch, rc, n, dev, sp)
+                             for n in ("X", "W", "bias", "dY", "preact"))
+    Y = torch.empty((Mg, Ng), dtype=bf, device=dev)
+    pre = torch.empty((Mg, Ng), dtype=bf, device=dev)
+    dX = torch.empty((Mg, Kg), dtype=bf, device=dev)
+    bgrad = torch.empty((Kg,), dtype=torch.float32, device=dev)
+    plan = {
+        "fwd": gf.gf_matmul_plan_ex(Mg, Ng, Kg, gf.GF_BF16, gf.GF_EPILOG_GELU_AUX_BIAS,
+                                    gf.GF_BIAS_COL, gf.GF_B_KN),
+        "bwd": gf.gf_matmul_plan_ex(Mg, Kg, Ng, gf.GF_BF16, gf.GF_EPILOG_DGELU_BGRAD,
+                                    gf.GF_BIAS_COL, gf.GF_B_NK),
+        "fwd_none": gf.gf_matmul_plan_ex(Mg, Ng, Kg, gf.GF_BF16, gf.GF_EPILOG_NONE,
+                                         gf.GF_BIAS_COL, gf.GF_B_KN),
+        "bwd_none": gf.gf_matmul_plan_ex(Mg, Kg, Ng, gf.GF_BF16, gf.GF_EPILOG_NONE,
+                                         gf.GF_BIAS_COL, gf.GF_B_NK),
+    }
+    # the bare GEMMs run in the fused plans' kernel and tile configuration
+    for a, b in (("fwd_none", "fwd"), ("bwd_none", "bwd")):
+        d = gf.gf_plan_describe(plan[b])
+        gf.gf_plan_set_option(plan[a], gf.GF_OPT_KERNEL, 2 if d["tile_m"] == 256 else 1)
+        if d["tile_m"] != 256:
+            gf.gf_plan_set_option(plan[a], gf.GF_OPT_TILE_N, d["tile_n"])
+    ex = gf.gf_matmul_execute
+
+    def unfused_fwd():
+        torch.addmm(bias, X, W, out=pre)
+        F.gelu(pre, approximate="tanh")
+
+    def unfused_bwd():
+        g = torch.matmul(dY, W.t())
+        dz = torch.ops.aten.gelu_backward(g, pre_b, approximate="tanh")
+        dz.float().sum(0)
+
+    fns = {
+        "fwd_gelu_aux_bias": lambda: ex(plan["fwd"], X, W, bias=bias, out=Y, aux_out=pre,
+                                        stream=sp),
+        "bwd_dgelu_bgrad": lambda: ex(plan["bwd"], dY, W, out=dX, aux_in=pre_b, bgrad=bgrad,
+                                      stream=sp),
+        "fwd_none": lambda: ex(plan["fwd_none"], X, W, out=Y, stream=sp),
+        "bwd_none": lambda: ex(plan["bwd_none"], dY, W, out=dX, stream=sp),
+        "torch_unfused_fwd": unfused_fwd,
+        "torch_unfused_bwd": unfused_bwd,
+    }
+    flop = 2.0 * Mg * Ng * Kg
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ms = _interleaved(torch, fns, reps=max(5, args.steps))
+    clk = clocks.stop()
+    ok = all(gf.gf_plan_status(p, sp) == gf.GF_OK for p in plan.values())
+    for p in plan.values():
+        p.free()
+    step = ms["fwd_gelu_aux_bias"] + ms["bwd_dgelu_bgrad"]
+    return {
+        "workload": f"gelu_bf16_fwd_gelu_aux_bias_bwd_dgelu_bgrad_{Mg}x{Ng}x{Kg}",
+        "value": 2 * flop / (step * 1e-3) / 1e12, "ms_per_step": step,
+        "pct_of_peak": 100 * 2 * flop / (step * 1e-3) / 1e12 / peak, "peak_source": pk,
+        "kernels_ms": ms,
+        "kernels_tflops": {k: flop / (v * 1e-3) / 1e12 for k, v in ms.items()},
+        "epilogue_overhead": {"fwd": ms["fwd_gelu_aux_bias"] / ms["fwd_none"] - 1,
+                              "bwd": ms["bwd_dgelu_bgrad"] / ms["bwd_none"] - 1},
+        "fused_vs_torch_unfused": {"fwd": ms["torch_unfused_fwd"] / ms["fwd_gelu_aux_bias"],
+                                   "bwd": ms["torch_unfused_bwd"] / ms["bwd_dgelu_bgrad"]},
+        "clocks": clk, "status_ok": ok,
+    }
+
+
+def run_swiglu_workload(args, gf, torch, dev, sp, peak, pk, Ms):
+    """SwiGLU MLP at H = 5120, I = 17408, bf16: the fused gate+up forward
+    (saving g and u), the down GEMM h Wd^T, and dh = dout Wd with the dSwiGLU
+    epilogue, for each M; against the same work unfused in torch (cuBLAS GEMMs
+    + elementwise ops) and against one bare GEMM x [Wg; Wu]^T of the same
+    flops."""
+    import torch.nn.functional as F
+    out = []
+    for Mw in Ms:
+        rc = synth.swiglu(Mw)
+        H = rc.tensors["x"].shape[1]
+        I = rc.tensors["Wg"].shape[0]
+        bf = torch.bfloat16
+        x = _dev_fill(torch, rc, "x", dev, sp)
+        Wgu = torch.empty((2 * I, H), dtype=bf, device=dev)
+        Wg = _dev_fill(torch, rc, "Wg", dev, sp, view=Wgu[:I])
+        Wu = _dev_fill(torch, rc, "Wu", dev, sp, view=Wgu[I:])
+        Wd = _dev_fill(torch, rc, "Wd", dev, sp)
+        dout = _dev_fill(torch, rc, "dout", dev, sp)
+        h, g, u, dgt, dup = (torch.empty((Mw, I), dtype=bf, device=dev) for _ in range(5))
+        o = torch.empty((Mw, H), dtype=bf, device=dev)
+        gu = torch.empty((Mw, 2 * I), dtype=bf, device=dev)
+        fwd = gf.gf_swiglu_plan(Mw, I, H, gf.GF_BF16, save_gu=True)
+        down = gf.gf_matmul_plan_ex(Mw, H, I, gf.GF_BF16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
+                                    gf.GF_B_NK)
+        bwd = gf.gf_dswiglu_plan(Mw, I, H, gf.GF_BF16)
+        bare = gf.gf_matmul_plan_ex(Mw, 2 * I, H, gf.GF_BF16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
+                                    gf.GF_B_NK)
+        dh_none = gf.gf_matmul_plan_ex(Mw, I, H, gf.GF_BF16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
+                                       gf.GF_B_KN)
+
+        def t_gateup():
+            gt = torch.matmul(x, Wg.t())
+            ut = torch.matmul(x, Wu.t())
+            return F.silu(gt) * ut
+
+        def t_dswiglu():
+            dh = torch.matmul(dout, Wd)
+            sg = torch.sigmoid(g)
+            return dh * u * sg * (1 + g * (1 - sg)), dh * (g * sg)
+
+        fns = {
+            "gate_up_swiglu": lambda: gf.gf_swiglu_execute(fwd, x, Wg, Wu, h, g, u, stream=sp),
+            "down_none": lambda: gf.gf_matmul_execute(down, h, Wd, out=o, stream=sp),
+            "dh_dswiglu": lambda: gf.gf_dswiglu_execute(bwd, dout, Wd, g, u, dgt, dup, stream=sp),
+            "gate_up_bare_gemm": lambda: gf.gf_matmul_execute(bare, x, Wgu, out=gu, stream=sp),
+            "dh_bare_gemm": lambda: gf.gf_matmul_execute(dh_none, dout, Wd, out=h, stream=sp),
+            "torch_gate_up_silu_mul": t_gateup,
+            "torch_dh_dswiglu": t_dswiglu,
+        }
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        ms = _interleaved(torch, fns, reps=max(5, args.steps))
+        clk = clocks.stop()
+        ok = all(gf.gf_plan_status(p, sp) == gf.GF_OK for p in (fwd, down, bwd, bare, dh_none))
+        for p in (fwd, down, bwd, bare, dh_none):
+            p.free()
+        f_gu, f_mm = 4.0 * Mw * I * H, 2.0 * Mw * I * H
+        flops = {"gate_up_swiglu": f_gu, "down_none": f_mm, "dh_dswiglu": f_mm,
+                 "gate_up_bare_gemm": f_gu, "dh_bare_gemm": f_mm,
+                 "torch_gate_up_silu_mul": f_gu, "torch_dh_dswiglu": f_mm}
+        step = ms["gate_up_swiglu"] + ms["down_none"] + ms["dh_dswiglu"]
+        v = (f_gu + 2 * f_mm) / (step * 1e-3) / 1e12
+        out.append({
+            "workload": f"swiglu_mlp_bf16_M{Mw}_H{H}_I{I}", "M": Mw,
+            "value": v, "ms_per_step": step, "pct_of_peak": 100 * v / peak, "peak_source": pk,
+            "kernels_ms": ms,
+            "kernels_tflops": {k: flops[k] / (t * 1e-3) / 1e12 for k, t in ms.items()},
+            "epilogue_overhead": {"gate_up": ms["gate_up_swiglu"] / ms["gate_up_bare_gemm"] - 1,
+                                  "dh": ms["dh_dswiglu"] / ms["dh_bare_gemm"] - 1},
+            "fused_vs_torch_unfused": {
+                "gate_up": ms["torch_gate_up_silu_mul"] / ms["gate_up_swiglu"],
+                "dh": ms["torch_dh_dswiglu"] / ms["dh_dswiglu"]},
+            "clocks": clk, "status_ok": ok,
+        })
+        del x, Wgu, Wg, Wu, Wd, dout, h, g, u, dgt, dup, o, gu
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_workload(args):
+    """`--workload gelu|swiglu`: the pages' other two workloads, one JSON line
+    each, with the fused kernels' throughput, the epilogue overhead against a
+    bare GEMM of the same flops and the unfused torch (cuBLAS + elementwise)
+    time of the same work."""
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+    gf.build()
+    synth.build_cuda()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sp = torch.cuda.current_stream().cuda_stream
+    pk_d, kind = peaks()
+    key = "bf16_tflops_sustained"
+    peak = float(pk_d.get(key) or FALLBACK[key])
+    pk = f"{kind} {key}"
+    if args.workload == "gelu":
+        lines = [run_gelu_workload(args, gf, torch, dev, sp, peak, pk)]
+    else:
+        Ms = [int(v) for v in args.swiglu_m.split(",")]
+        lines = run_swiglu_workload(args, gf, torch, dev, sp, peak, pk, Ms)
+    for ln in lines:
+        print(json.dumps({"metric": METRIC, "unit": "TFLOP/s", "dtype": "bf16",
+                          "data": "synthetic", "higher_is_better": True, **ln}), flush=True)
+    return 0 if all(ln["status_ok"] for ln in lines) else 1
+
+
 def run_compare_schedules(args):
     """Steady-state comparison of the CTA-pair kernel's tile schedules on the
     full-size fused forward, and torch.matmul (cuBLAS, no epilogue) for
@@ -657,6 +869,9 @@ def main():
     ap.add_argument("--autotune", action="store_true",
                     help="let gf_matmul_autotune pick the kernels before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="linear_pair", choices=["linear_pair", "gelu", "swiglu"],
+                    help="gelu / swiglu: the other two workloads, one JSON line each")
+    ap.add_argument("--swiglu-m", default="2048,8192,16384")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gf":
         args.warmup = 3
@@ -666,6 +881,8 @@ def main():
         return run_profile_case(args)
     if args.compare_schedules:
         return run_compare_schedules(args)
+    if args.workload != "linear_pair":
+        return run_workload(args)
     return run_gpu(args)
 
 
