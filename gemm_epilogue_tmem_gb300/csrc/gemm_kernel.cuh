@@ -95,23 +95,32 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
   for (int i = 0; i < 8; ++i) f[i] = to_f32<T>(h[i]);
 }
 
+// Hardware tanh (tanh.approx.f32, relative error about 2^-11: below the
+// rounding of the 16-bit outputs these epilogues store).
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear Units",
 // 2016): 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))), and its derivative.
 __device__ __forceinline__ float gelu_tanh(float z) {
   const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
-  return 0.5f * z * (1.f + tanhf(u));
+  return 0.5f * z * (1.f + tanh_fast(u));
 }
 
 __device__ __forceinline__ float dgelu_tanh(float z) {
   const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
-  const float t = tanhf(u);
+  const float t = tanh_fast(u);
   return 0.5f * (1.f + t) +
          0.5f * z * (1.f - t * t) * 0.7978845608028654f * (1.f + 3.f * 0.044715f * z * z);
 }
 
 // SiLU and the logistic function of the SwiGLU epilogues (gate+up
-// forward, dSwiGLU backward): sigmoid(g) = 1 / (1 + e^-g), silu(g) = g sigmoid(g).
-__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.f, 1.f + __expf(-g)); }
+// forward, dSwiGLU backward): sigmoid(g) = 1 / (1 + e^-g) = (1 + tanh(g/2)) / 2,
+// silu(g) = g sigmoid(g).
+__device__ __forceinline__ float sigmoid_f(float g) { return fmaf(0.5f, tanh_fast(0.5f * g), 0.5f); }
 
 __device__ __forceinline__ float silu_f(float g) { return g * sigmoid_f(g); }
 
@@ -440,7 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile_coords(p, t, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
         const int nbox = B_MN ? min(BN / 64, (p.N - n0 + 63) / 64) : 1;
-        const uint32_t bytes = C::kABytes + (B_MN ? nbox * 64 * kBK * 2 : C::kStageBBytes);
+        // a 3-D box always moves all BN / 64 chunks (zero fill past N)
+        const uint32_t bytes =
+            C::kABytes + (B_MN && !p.b_mn_3d ? nbox * 64 * kBK * 2 : C::kStageBBytes);
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
@@ -452,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = full0 + 8u * stage;
             mbar_arrive_expect_tx(fb, bytes);
             tma_load(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0, p.l2_hint_a, pol_a);
-            if (B_MN) {
+            if (B_MN && p.b_mn_3d) {
+              tma_load_3d(sB + stage * C::kStageBBytes, &tmB, fb, 0, kb * kBK, n0 / 64);
+            } else if (B_MN) {
               for (int j = 0; j < nbox; ++j)
                 tma_load(sB + stage * C::kStageBBytes + j * (64 * kBK * 2), &tmB, fb, n0 + 64 * j,
                          kb * kBK, p.l2_hint_b, pol_b);

@@ -1,11 +1,15 @@
 // CTA-pair variant of the fused GEMM + epilogue kernel: a cluster of two
 // CTAs on two SMs computes one 256 x 256 output tile with
-// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction); with
-// two B operands (gate+up SwiGLU) a 256 x 128 tile of each, N = 128.
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per instruction).
 //
 //   - Each CTA loads its own 128 rows of A and its own half of the B columns
 //     for every k-slice (TMA, 128-byte swizzle, no multicast): per SM the
 //     operand traffic per flop is 2/3 of the single-CTA 128 x 256 tile's.
+//   - Two B operands (gate+up SwiGLU): the pair's "halves" of B are the two
+//     weights -- rank 0 loads 128 rows of the gate weight, rank 1 the same
+//     rows of the up weight -- so one N = 256 MMA puts g in accumulator
+//     columns 0..127 and u in 128..255 of every row: a 256 x 128 output tile
+//     at the MMA rate of the single-operand kernel.
 //   - The stage-full barrier lives in the leader CTA (rank 0): the leader's
 //     producer expects the bytes of both CTAs, the peer's TMA loads signal
 //     the leader's barrier (.cta_group::2).
@@ -31,11 +35,12 @@ namespace gf {
 // RED = the epilog reduces a bias gradient and needs the [4][BN] scratch.
 template <int NB = 1, bool RED = false>
 struct PairCfg {
-  static constexpr int BN = NB == 2 ? 128 : 256;       // pair tile 256 x BN per B operand
+  static constexpr int BN = NB == 2 ? 128 : 256;       // output columns of a pair tile
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
-  static constexpr int kBBytes = (BN / 2) * kBK * 2;   // this CTA's BN/2 columns of one B
-  static constexpr int kStageBBytes = NB * kBBytes;    // 16 KB either way
-  static constexpr int kAccCols = NB * BN;             // TMEM columns of one accumulator set
+  // 16 KB: this CTA's 128 of the tile's 256 B columns, or (two operands) the
+  // tile's 128 columns of this CTA's operand
+  static constexpr int kStageBBytes = 128 * kBK * 2;
+  static constexpr int kAccCols = 256;                 // TMEM columns of one accumulator (N)
   static constexpr int kTmemCols = 2 * kAccCols;       // two accumulator buffers
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
   static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
@@ -200,8 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < 0) break;
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
-        const int m_row = mb2 * 256 + 128 * (int)rank;     // this CTA's A rows
-        const int n_col = nb * BN + (BN / 2) * (int)rank;  // this CTA's B columns
+        const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
+        // this CTA's B columns (two operands: the tile's columns of its own operand)
+        const int n_col = NB == 2 ? nb * BN : nb * BN + (BN / 2) * (int)rank;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
@@ -215,15 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
             if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kStageBBytes));
             tma_load_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row, ha, pol_a);
-            if (B_MN) {
+            if (B_MN && p.b_mn_3d) {
+              tma_load_3d_pair(sB + stage * C::kStageBBytes, &tmB, fb, 0, kb * kBK, n_col / 64);
+            } else if (B_MN) {
               tma_load_pair(sB + stage * C::kStageBBytes, &tmB, fb, n_col, kb * kBK, hb, pol_b);
               tma_load_pair(sB + stage * C::kStageBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
                             kb * kBK, hb, pol_b);
             } else {
-              tma_load_pair(sB + stage * C::kStageBBytes, &tmB, fb, kb * kBK, n_col, hb, pol_b);
-              if (NB == 2)
-                tma_load_pair(sB + stage * C::kStageBBytes + C::kBBytes, &tmB2, fb, kb * kBK,
-                              n_col, hb, pol_b);
+              tma_load_pair(sB + stage * C::kStageBBytes, NB == 2 && rank == 1 ? &tmB2 : &tmB, fb,
+                            kb * kBK, n_col, hb, pol_b);
             }
             issued[stage] = (int)phase;
           }
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA (leader)
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_f16(kBf16, B_MN, 256, BN);
+      constexpr uint32_t idesc = idesc_f16(kBf16, B_MN, 256, 256);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -289,10 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
             umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-            if constexpr (NB == 2) {
-              const uint64_t bdesc2 = sdesc_sw128(b_base + C::kBBytes + kk * 32, 16, 1024);
-              umma_f16_pair(d_tmem + BN, adesc, bdesc2, idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
           }
           umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
           if (++stage == S) {

@@ -75,6 +75,8 @@ struct GemmParams {
   int32_t l2_hint_a;  // L2 policy of the A loads: 0 none, 1 evict first, 2 evict last
   int32_t l2_hint_b;  // ... of the B loads
   int* tile_counter;  // CTA-pair kernel: global tile counter of the dynamic schedule (null: static)
+  int32_t b_mn_3d;    // MN-major B through a 3-D map: one box per k-slice brings every
+                      // 64-column chunk of the tile (0: one 2-D box per chunk)
 };
 
 }  // namespace gf

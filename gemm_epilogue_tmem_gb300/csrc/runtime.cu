@@ -112,6 +112,24 @@ bool needs_aux_out(int e) {
 }
 bool needs_aux_in(int e) { return has_bgrad(e) || e == gf::EPI_DSWIGLU; }
 
+// 3-D tensor map over a row-major [k, n] matrix of 16-bit elements seen as
+// [n / 64][k][64]: a box of 64 x box_k x chunks brings `chunks` consecutive
+// 64-column (128-byte) chunks of box_k rows, chunk after chunk, the layout of
+// the MN-major operand in shared memory. n must be a multiple of 64.
+bool encode_mn_3d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t n, uint64_t k,
+                  uint32_t box_k, uint32_t chunks) {
+  cuuint64_t dims[3] = {64, k, n / 64};
+  cuuint64_t strides[2] = {n * 2, 128};
+  cuuint32_t box[3] = {64, box_k, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dt == GF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D tensor map over a row-major [outer, inner] matrix of 16-bit elements,
 // boxes of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
 bool encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner, uint64_t outer,
@@ -333,17 +351,24 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   }
 
   CUtensorMap tmA, tmB, tmB2;
+  bool b_mn_3d = false;
   memset(&tmA, 0, sizeof tmA);
   memset(&tmB, 0, sizeof tmB);
   memset(&tmB2, 0, sizeof tmB2);
   if (p->k > 0) {
     if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
-    // K-major B boxes: a pair CTA loads half of the tile's columns
-    const uint32_t rows_nk = p->pair ? static_cast<uint32_t>(p->tile_n / 2)
-                                     : static_cast<uint32_t>(p->tile_n);
-    const bool ok = p->b_layout == GF_B_KN
-                        ? encode_2d(&tmB, x.B, p->dtype, p->n, p->k, 64, 64)
-                        : encode_2d(&tmB, x.B, p->dtype, p->k, p->n, 64, rows_nk);
+    // K-major B boxes: a pair CTA loads half of the tile's columns, or with
+    // two B operands all of the tile's columns of one operand
+    const uint32_t rows_nk = p->pair && !dual ? static_cast<uint32_t>(p->tile_n / 2)
+                                              : static_cast<uint32_t>(p->tile_n);
+    // MN-major B: one 3-D box per k-slice for all of this CTA's column
+    // chunks when n is a multiple of 64, else one 2-D box per chunk
+    b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 && p->l2_hint_b == 0 &&
+              encode_mn_3d(&tmB, x.B, p->dtype, p->n, p->k, 64, rows_nk / 64);
+    const bool ok = b_mn_3d ||
+                    (p->b_layout == GF_B_KN
+                         ? encode_2d(&tmB, x.B, p->dtype, p->n, p->k, 64, 64)
+                         : encode_2d(&tmB, x.B, p->dtype, p->k, p->n, 64, rows_nk));
     if (!ok) return fail(GF_ERR_INVALID_VALUE);
     if (dual && !encode_2d(&tmB2, x.B2, p->dtype, p->k, p->n, 64, rows_nk))
       return fail(GF_ERR_INVALID_VALUE);
@@ -371,6 +396,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.drop_load = p->drop_load;
   prm.l2_hint_a = p->l2_hint_a;
   prm.l2_hint_b = p->l2_hint_b;
+  prm.b_mn_3d = b_mn_3d ? 1 : 0;
   if (p->pair && !p->static_schedule && !p->one_tile_per_cta) {
     // the tile counter sits in the plan's status block, 64 bytes past the status word
     prm.tile_counter = p->d_status + 16;
