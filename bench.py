@@ -343,6 +343,9 @@ def run_gpu(args):
     bwd_none = gf.gf_matmul_plan_ex(M, K, N, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
                                     gf.GF_B_NK)
     launches_per_step = 3  # fused forward, fused backward, bgrad finalize
+    if args.kernel:
+        for pl in (fwd, bwd, fwd_none, bwd_none):
+            gf.gf_plan_set_option(pl, gf.GF_OPT_KERNEL, args.kernel)
     if args.autotune:
         gf.gf_matmul_autotune(fwd, X, W, bias=bias, out=Y, aux_out=aux, stream=sp, reps=2)
         gf.gf_matmul_autotune(bwd, dY, W, out=dZ, aux_in=mask, bgrad=bgrad, stream=sp, reps=2)
@@ -801,10 +804,11 @@ def run_compare_schedules(args):
     synth.dev_normal(bias, synth.F16, 0, synth.TID_BIAS, 0.1, sp)
     torch.cuda.synchronize()
     cfgs = {}
-    for name, sched in (("dynamic", 2), ("static", 3), ("one_tile_per_pair", 1)):
+    for name, sched, kern in (("dynamic", 2, 2), ("static", 3, 2), ("one_tile_per_pair", 1, 2),
+                              ("wide_256x512_dynamic", 2, 3)):
         plan = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL,
                                     gf.GF_B_KN)
-        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, kern)
         gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, sched)
         cfgs[name] = (plan, (lambda p: lambda: gf.gf_matmul_execute(
             p, X, W, bias=bias, out=Y, aux_out=aux, stream=sp))(plan))
@@ -854,7 +858,8 @@ def main():
                     help="M,N,K: run one fused GEMM of this shape (for ncu captures)")
     ap.add_argument("--epilog", default="relu_aux_bias",
                     choices=["relu_aux_bias", "drelu_bgrad", "none", "relu_bias"])
-    ap.add_argument("--kernel", type=int, default=0, help="0 plan's choice, 1 single CTA, 2 pair")
+    ap.add_argument("--kernel", type=int, default=0,
+                    help="0 plan's choice, 1 single CTA, 2 pair, 3 pair with 256 x 512 tiles")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)

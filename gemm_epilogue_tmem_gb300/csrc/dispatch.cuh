@@ -22,10 +22,10 @@ cudaError_t launch_instance(const LaunchArgs& a) {
   return cudaGetLastError();
 }
 
-template <int EPI, typename T, bool B_MN>
+template <int EPI, typename T, bool B_MN, bool WIDE = false>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
-  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kSmemBytes;
+  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE>;
+  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -75,7 +75,7 @@ int pair_max_clusters() {
 // two-B-operand epilogs: B given [n, k] (K-major), 128-wide single-CTA tiles or CTA pairs
 template <int EPI>
 cudaError_t launch_dual(const LaunchArgs& a) {
-  if (a.b_mn) return cudaErrorInvalidValue;
+  if (a.b_mn || a.wide) return cudaErrorInvalidValue;
   if (a.pair)
     return a.bf16 ? launch_pair_instance<EPI, __nv_bfloat16, false>(a)
                   : launch_pair_instance<EPI, __half, false>(a);
@@ -85,6 +85,13 @@ cudaError_t launch_dual(const LaunchArgs& a) {
 
 template <int EPI>
 cudaError_t launch_epi(const LaunchArgs& a) {
+  if (a.pair && a.wide) {
+    if (a.bf16)
+      return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true, true>(a)
+                    : launch_pair_instance<EPI, __nv_bfloat16, false, true>(a);
+    return a.b_mn ? launch_pair_instance<EPI, __half, true, true>(a)
+                  : launch_pair_instance<EPI, __half, false, true>(a);
+  }
   if (a.pair) {
     if (a.bf16)
       return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true>(a)

@@ -162,7 +162,9 @@ __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* a
 // Drain one 128-row x BN accumulator from tensor memory and apply the
 // epilog. Warp quarter q owns TMEM lanes 32q..32q+31 = output rows
 // row0 + 32q + lane; t_row addresses (lane 32q, first column of the buffer).
-template <int EPI, typename T, int BN>
+// A bias-gradient epilog leaves the warp's 32-row column sums in
+// red[q * RS + column] (RS = BN unless the caller drains a wider tile in parts).
+template <int EPI, typename T, int BN, int RS = BN>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red) {
   const int row = row0 + 32 * q + (int)lane;
@@ -349,7 +351,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
           v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
         }
       }
-      red[q * BN + 32 * c + (int)lane] = v[0];
+      red[q * RS + 32 * c + (int)lane] = v[0];
     }
   }
 }

@@ -24,6 +24,15 @@
 //     memory. Dynamic keeps the tiles in flight a contiguous run of the
 //     raster order, so operand panels shared by neighbouring tiles are read
 //     from HBM about once instead of once per drifting pair.
+//   - Wide tiles (WIDE): 256 x 512 per pair, two N = 256 MMAs per k-step
+//     into the two halves of one 512-column accumulator. A k-slice of A then
+//     feeds twice the flops, so a stage brings 48 KB per 1024 MMA cycles per
+//     SM instead of 32 KB per 512: 3/4 of the operand bytes per flop, for
+//     SMs whose tensor-copy ingress, not the tensor pipe, sets the pace of
+//     the 256-wide tile. The price is a single accumulator: the epilogue
+//     drains half 0 and releases it, then half 1; the MMA thread starts the
+//     next tile on half 0 over the stages already loaded and adds the half-1
+//     products of those stages once half 1 is free.
 //   - Teardown: drains, then a cluster barrier, then a pair TMEM dealloc.
 #pragma once
 
@@ -31,17 +40,21 @@
 
 namespace gf {
 
-// NB = number of B operands: 1, or 2 for the gate+up SwiGLU (two accumulators);
-// RED = the epilog reduces a bias gradient and needs the [4][BN] scratch.
-template <int NB = 1, bool RED = false>
+// NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
+// side in one accumulator); RED = the epilog reduces a bias gradient and
+// needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only).
+template <int NB = 1, bool RED = false, bool WIDE = false>
 struct PairCfg {
-  static constexpr int BN = NB == 2 ? 128 : 256;       // output columns of a pair tile
+  static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
+  static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
-  // 16 KB: this CTA's 128 of the tile's 256 B columns, or (two operands) the
-  // tile's 128 columns of this CTA's operand
-  static constexpr int kStageBBytes = 128 * kBK * 2;
-  static constexpr int kAccCols = 256;                 // TMEM columns of one accumulator (N)
-  static constexpr int kTmemCols = 2 * kAccCols;       // two accumulator buffers
+  // one 16 KB B part: this CTA's 128 of an MMA's 256 B columns, or (two
+  // operands) the tile's 128 columns of this CTA's operand; wide: two parts
+  static constexpr int kBPartBytes = 128 * kBK * 2;
+  static constexpr int kStageBBytes = (WIDE ? 2 : 1) * kBPartBytes;
+  static constexpr int kAccCols = WIDE ? 512 : 256;    // TMEM columns of one accumulator
+  static constexpr int kNumAcc = WIDE ? 1 : 2;         // accumulator buffers
+  static constexpr int kTmemCols = kNumAcc * kAccCols; // 512 either way
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
   static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes);
@@ -71,13 +84,13 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-template <int EPI, typename T, bool B_MN>
+template <int EPI, typename T, bool B_MN, bool WIDE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = PairCfg<NB, epi_has_bgrad(EPI)>;
+  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -92,8 +105,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gctrl = gbase + (ctrl - base);
   const uint32_t full0 = ctrl;              // leader: S barriers, stage filled (both CTAs' bytes)
   const uint32_t empty0 = ctrl + 8u * S;    // both: S barriers, stage consumed
-  const uint32_t tfull0 = ctrl + 16u * S;   // both: 2 barriers, accumulator ready
-  const uint32_t tempty0 = tfull0 + 16u;    // leader: 2 barriers, accumulator drained (8 warps)
+  // both: 2 barriers, accumulator buffer ready (wide: only the first is used)
+  const uint32_t tfull0 = ctrl + 16u * S;
+  // leader: 2 barriers, accumulator buffer drained by the 8 epilogue warps
+  // (wide: half 0 drained, half 1 drained)
+  const uint32_t tempty0 = tfull0 + 16u;
   const uint32_t done_bar = tempty0 + 16u;  // leader: MMA teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gctrl + 16 * S + 40);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 44);
@@ -206,8 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
         const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
-        // this CTA's B columns (two operands: the tile's columns of its own operand)
-        const int n_col = NB == 2 ? nb * BN : nb * BN + (BN / 2) * (int)rank;
+        // this CTA's B columns (two operands: the tile's columns of its own
+        // operand; wide: part h at n_col + 256 h)
+        const int n_col = NB == 2 ? nb * BN : nb * BN + 128 * (int)rank;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
@@ -221,15 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = mapa_shared(fb_local, 0);  // the leader's barrier
             if (leader) mbar_arrive_expect_tx(fb_local, 2u * (C::kABytes + C::kStageBBytes));
             tma_load_pair(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m_row, ha, pol_a);
-            if (B_MN && p.b_mn_3d) {
-              tma_load_3d_pair(sB + stage * C::kStageBBytes, &tmB, fb, 0, kb * kBK, n_col / 64);
-            } else if (B_MN) {
-              tma_load_pair(sB + stage * C::kStageBBytes, &tmB, fb, n_col, kb * kBK, hb, pol_b);
-              tma_load_pair(sB + stage * C::kStageBBytes + 64 * kBK * 2, &tmB, fb, n_col + 64,
-                            kb * kBK, hb, pol_b);
-            } else {
-              tma_load_pair(sB + stage * C::kStageBBytes, NB == 2 && rank == 1 ? &tmB2 : &tmB, fb,
-                            kb * kBK, n_col, hb, pol_b);
+#pragma unroll
+            for (int h = 0; h < (WIDE ? 2 : 1); ++h) {
+              const uint32_t dst = sB + stage * C::kStageBBytes + h * C::kBPartBytes;
+              const int col = n_col + 256 * h;
+              if (B_MN && p.b_mn_3d) {
+                tma_load_3d_pair(dst, &tmB, fb, 0, kb * kBK, col / 64);
+              } else if (B_MN) {
+                tma_load_pair(dst, &tmB, fb, col, kb * kBK, hb, pol_b);
+                tma_load_pair(dst + 64 * kBK * 2, &tmB, fb, col + 64, kb * kBK, hb, pol_b);
+              } else {
+                tma_load_pair(dst, NB == 2 && rank == 1 ? &tmB2 : &tmB, fb, kb * kBK, col, hb,
+                              pol_b);
+              }
             }
             issued[stage] = (int)phase;
           }
@@ -265,8 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         if (t < 0) break;
-        const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        // double buffer: tile it uses buffer it & 1, whose previous use (tile
+        // it - 2) must be drained; wide: one buffer in two halves, released
+        // by the epilogue of tile it - 1 one after the other
+        const int buf = WIDE ? 0 : (it & 1);
+        const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded_cluster(tempty0 + 8u * buf, use ^ 1u, abort_flag,
                                        p.wait_limit_ns)) {
           raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
@@ -276,10 +300,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * C::kAccCols);
         if (p.num_k_blocks == 0) {
+          if (WIDE &&
+              !mbar_wait_bounded_cluster(tempty0 + 8u, use ^ 1u, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
+            aborted = true;
+            break;
+          }
           umma_commit_pair(tfull0 + 8u * buf, 0x3);  // nothing to multiply: acc is zero
           continue;
         }
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        // the MMAs of one k-slice into accumulator half h (wide) or the whole
+        // accumulator
+        auto mma_kslice = [&](int st, int kb, int h) {
+          const uint32_t a_base = sA + st * C::kABytes;
+          const uint32_t b_base = sB + st * C::kStageBBytes + h * C::kBPartBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
+                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_f16_pair(d_tmem + 256u * (uint32_t)h, adesc, bdesc, idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+          }
+        };
+        int kb = 0;
+        if constexpr (WIDE) {
+          // half 0 over the first stages that the producer has loaded while
+          // the previous tile drained, then half 1 of the same stages
+          const int pre = p.num_k_blocks < S ? p.num_k_blocks : S;
+          int st = stage;
+          uint32_t ph = phase;
+          for (int j = 0; j < pre && ok; ++j) {
+            if (!mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, p.wait_limit_ns)) {
+              raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
+              ok = false;
+              aborted = true;
+              break;
+            }
+            tc_fence_after();
+            mma_kslice(st, j, 0);
+            if (++st == S) {
+              st = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (!mbar_wait_bounded_cluster(tempty0 + 8u, use ^ 1u, abort_flag, p.wait_limit_ns)) {
+            raise_error(p, abort_flag, ST_TIMEOUT_MMA_TMEM);
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          for (int j = 0; j < pre; ++j) {
+            mma_kslice(stage, j, 1);
+            umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          kb = pre;
+        }
+        for (; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
             ok = false;
@@ -287,15 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = sA + stage * C::kABytes;
-          const uint32_t b_base = sB + stage * C::kStageBBytes;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = sdesc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
-                                        : sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
+          mma_kslice(stage, kb, 0);
+          if constexpr (WIDE) mma_kslice(stage, kb, 1);
           umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
           if (++stage == S) {
             stage = 0;
@@ -329,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t < 0) break;
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      const int buf = WIDE ? 0 : (it & 1);
+      const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
       ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
       if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
       if (!ok) {
@@ -345,10 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = nb * BN;
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
-      epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
+      if constexpr (WIDE) {
+        // half 0, release it (the next tile's first MMAs go there), half 1
+        epilogue_drain<EPI, T, 256, BN>(p, t_row, row0, n0, q, lane, red);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader);
+        epilogue_drain<EPI, T, 256, BN>(p, t_row + 256u, row0, n0 + 256, q, lane, red + 256);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
+      } else {
+        epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
+      }
       if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN>(p, red, ep_tid, n0, row0 / kBM);
     }
   }

@@ -12,6 +12,8 @@ int stages_for(int tile_n, int pair, int epi) {
   if (epi_dual(epi))
     return pair ? (red ? PairCfg<2, true>::kStages : PairCfg<2, false>::kStages)
                 : (red ? TileCfg<128, 2, true>::kStages : TileCfg<128, 2, false>::kStages);
+  if (pair && tile_n == 512)
+    return red ? PairCfg<1, true, true>::kStages : PairCfg<1, false, true>::kStages;
   if (pair) return red ? PairCfg<1, true>::kStages : PairCfg<1, false>::kStages;
   if (tile_n == 256) return red ? TileCfg<256, 1, true>::kStages : TileCfg<256, 1, false>::kStages;
   return red ? TileCfg<128, 1, true>::kStages : TileCfg<128, 1, false>::kStages;

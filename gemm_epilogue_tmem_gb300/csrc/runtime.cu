@@ -32,12 +32,13 @@ struct gf_plan {
   int num_sms;
   int tile_n;
   int forced_tile_n;
-  int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair
+  int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair, 3 CTA pair with 256 x 512 tiles
   int forced_group_m;    // 0 auto, else row blocks per raster group
   int l2_hint_a, l2_hint_b;  // L2 eviction policy of the A / B loads (0 none, 1 first, 2 last)
   int one_tile_per_cta;  // 1: grid of one tile per CTA (pair); the hardware orders the tiles
   int static_schedule;   // 1: persistent CTA pairs walk every gridDim-th tile (default: counter)
   int pair;              // the plan uses the CTA-pair kernel
+  int wide;              // ... with 256 x 512 tiles
   int max_pair_clusters; // resident CTA pairs (0: the pair kernel cannot run)
   int stages;
   int grid;
@@ -156,15 +157,20 @@ void plan_tiles(gf_plan* p) {
   // with two B operands) moves 2/3 of the operand bytes per flop of the
   // single-CTA tile; take it when its tiles fill the resident pairs, else the
   // single-CTA kernel with the tile width that keeps the SMs busy.
-  const int pair_n = dual ? 128 : 256;
+  // Wide pair tiles (256 x 512, forced_kernel 3) need 3/4 of the operand
+  // bytes per flop of the 256 x 256 pair tile but expose part of each
+  // epilogue; one B operand only.
+  const bool wide = p->forced_kernel == 3 && !dual && p->max_pair_clusters > 0;
+  const int pair_n = wide ? 512 : (dual ? 128 : 256);
   const int64_t pair_tiles = ((p->m + 255) / 256) * ((p->n + pair_n - 1) / pair_n);
   bool pair = false;
-  if (p->forced_kernel == 2)
+  if (p->forced_kernel == 2 || p->forced_kernel == 3)
     pair = p->max_pair_clusters > 0;
   else if (p->forced_kernel == 0)
     pair = p->max_pair_clusters > 0 && p->forced_tile_n == 0 && p->m > 128 &&
            pair_tiles >= p->max_pair_clusters;
   p->pair = pair ? 1 : 0;
+  p->wide = pair && wide ? 1 : 0;
   if (pair) {
     p->tile_n = pair_n;
     p->stages = gf::stages_for(pair_n, 1, p->epi);
@@ -272,7 +278,7 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
   p->forced_tile_n = env_tile && (atoi(env_tile) == 128 || atoi(env_tile) == 256) ? atoi(env_tile) : 0;
   const char* env_kernel = getenv("GF_KERNEL");
   p->forced_kernel = env_kernel ? atoi(env_kernel) : 0;
-  if (p->forced_kernel < 0 || p->forced_kernel > 2) p->forced_kernel = 0;
+  if (p->forced_kernel < 0 || p->forced_kernel > 3) p->forced_kernel = 0;
   p->max_pair_clusters = gf::pair_max_clusters_any();
   cudaGetLastError();
   plan_tiles(p);
@@ -359,8 +365,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
     if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
     // K-major B boxes: a pair CTA loads half of the tile's columns, or with
     // two B operands all of the tile's columns of one operand
-    const uint32_t rows_nk = p->pair && !dual ? static_cast<uint32_t>(p->tile_n / 2)
-                                              : static_cast<uint32_t>(p->tile_n);
+    const uint32_t rows_nk = p->pair && !dual ? 128u : static_cast<uint32_t>(p->tile_n);
     // MN-major B: one 3-D box per k-slice for all of this CTA's column
     // chunks when n is a multiple of 64, else one 2-D box per chunk
     b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 && p->l2_hint_b == 0 &&
@@ -422,6 +427,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   la.b_mn = p->b_layout == GF_B_KN ? 1 : 0;
   la.tile_n = p->tile_n;
   la.pair = p->pair;
+  la.wide = p->wide;
   la.stream = st;
 
   cudaError_t err;
@@ -526,8 +532,9 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       plan_tiles(p);
       return GF_OK;
     case GF_OPT_KERNEL:
-      if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
-      if (value == 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
+      if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
+      if (value >= 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
+      if (value == 3 && gf::epi_dual(p->epi)) return fail(GF_ERR_UNSUPPORTED);
       p->forced_kernel = static_cast<int>(value);
       plan_tiles(p);
       return GF_OK;
@@ -564,9 +571,11 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
   if (p->m == 0 || p->n == 0) return GF_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   ExecArgs x = {A, B, nullptr, bias, out, aux_in, nullptr, aux_out, nullptr, bgrad};
-  // candidates: {kernel (1 single, 2 pair), tile_n, schedule, group_m}
+  // candidates: {kernel (1 single, 2 pair, 3 pair with 256 x 512 tiles), tile_n, schedule,
+  // group_m}
   struct Cand { int kernel, tile_n, schedule, group_m; };
   const Cand cands[] = {{2, 0, 2, 8}, {2, 0, 2, 4}, {2, 0, 2, 16}, {2, 0, 3, 8},
+                        {3, 0, 2, 8}, {3, 0, 2, 16}, {3, 0, 2, 4},
                         {1, 256, 0, 8}, {1, 128, 0, 8}, {1, 256, 0, 4}};
   const int saved[5] = {p->forced_kernel, p->forced_tile_n, p->one_tile_per_cta,
                         p->static_schedule, p->forced_group_m};
@@ -577,7 +586,8 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
   Cand best = cands[0];
   gf_status st_out = GF_OK;
   for (const Cand& c : cands) {
-    if (c.kernel == 2 && p->max_pair_clusters == 0) continue;
+    if (c.kernel >= 2 && p->max_pair_clusters == 0) continue;
+    if (c.kernel == 3 && gf::epi_dual(p->epi)) continue;
     p->forced_kernel = c.kernel;
     p->forced_tile_n = c.tile_n;
     p->one_tile_per_cta = 0;

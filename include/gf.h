@@ -229,7 +229,11 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  * GF_OPT_KERNEL          : 0 the plan's choice, 1 the single-CTA kernel
  *                          (128 x tile_n tiles), 2 the CTA-pair kernel
  *                          (256 x 256 tiles on two SMs; GF_ERR_UNSUPPORTED if
- *                          it cannot be resident on this device).
+ *                          it cannot be resident on this device), 3 the
+ *                          CTA-pair kernel with 256 x 512 tiles (3/4 of the
+ *                          operand traffic per flop, one accumulator whose
+ *                          epilogue is partly exposed; not for the SwiGLU
+ *                          plans: GF_ERR_UNSUPPORTED).
  * Returns GF_ERR_INVALID_VALUE for an unknown option or value.
  */
 typedef enum gf_option {
@@ -265,8 +269,9 @@ GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t val
  * the nvmath-python / cuBLASLt page, "limitations" paragraph: autotuning
  * through MatmulPlanPreferences; here a search over this library's own
  * kernels). Runs the planned product once per candidate (CTA-pair kernel
- * with dynamic or static schedule and raster groups of 4, 8 or 16 tile rows;
- * single-CTA kernel with 256- or 128-wide tiles) on the caller's buffers,
+ * with 256- or 512-wide tiles, dynamic or static schedule and raster groups
+ * of 4, 8 or 16 tile rows; single-CTA kernel with 256- or 128-wide tiles) on
+ * the caller's buffers,
  * `reps` timed launches each after one warm-up, synchronising `stream`, and
  * keeps the fastest in the plan. The outputs hold the result of the last
  * launch. Arguments as gf_matmul_execute; reps in 1..100.
