@@ -141,6 +141,65 @@ __device__ __forceinline__ void store_row32(T* dst, const float* v, int col0, in
   }
 }
 
+// 32 x 32 bit-matrix transpose across a warp (lane i holds row i): five
+// butterfly stages, each swapping the off-diagonal s x s blocks between lanes
+// i and i ^ s with one shuffle. Returns column `lane`: bit i = bit `lane` of
+// lane i's input. Called by all 32 lanes.
+__device__ __forceinline__ uint32_t bit_transpose32(uint32_t x, uint32_t lane) {
+  const uint32_t lo[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const int sh = 16 >> k;
+    const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, sh);
+    x = (lane & (uint32_t)sh) ? ((x & ~lo[k]) | ((y >> sh) & lo[k]))
+                              : ((x & lo[k]) | ((y << sh) & ~lo[k]));
+  }
+  return x;
+}
+
+// The same 32 columns for all 32 rows of a warp (lane l holds row row0w + l),
+// through a 2 KB shared-memory transpose at `stg`: each global store
+// instruction then writes 8 rows x 64 contiguous bytes instead of 32 rows x
+// 16 bytes. The 16-byte pieces of a staged row are XOR-permuted by
+// (row / 2) % 4 so that both the row-wise writes and the piece-wise reads hit
+// 8 distinct 16-byte bank groups. Rows at or past M and columns at or past N
+// (a multiple of 8) are not written. Called by all 32 lanes.
+template <typename T>
+__device__ __forceinline__ void store_rows32_staged(T* base, int M, int N, int row0w, int col0,
+                                                    const float* v, uint32_t lane, uint32_t stg) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack2<T>(v[2 * i], v[2 * i + 1]);
+  const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+  for (uint32_t pc = 0; pc < 4; ++pc)
+    st_shared_v4(stg + lane * 64u + ((pc ^ sw) << 4), w[4 * pc], w[4 * pc + 1], w[4 * pc + 2],
+                 w[4 * pc + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const uint32_t r = 8u * g + (lane >> 2);
+    const uint32_t pc = lane & 3u;
+    const uint4 val = ld_shared_v4(stg + r * 64u + ((pc ^ ((r >> 1) & 3u)) << 4));
+    const int row = row0w + (int)r;
+    const int col = col0 + 8 * (int)pc;
+    if (row < M && col < N) *reinterpret_cast<uint4*>(base + (size_t)row * N + col) = val;
+  }
+  __syncwarp();
+}
+
+// this lane's 32 values of row `row` (direct) or the warp's 32 rows (staged)
+template <typename T, bool STG>
+__device__ __forceinline__ void emit_row32(T* base, int M, int N, int row0w, int col0,
+                                           const float* v, uint32_t lane, uint32_t stg) {
+  if constexpr (STG) {
+    store_rows32_staged<T>(base, M, N, row0w, col0, v, lane, stg);
+  } else {
+    const int row = row0w + (int)lane;
+    if (row < M) store_row32<T>(base + (size_t)row * N + col0, v, col0, N);
+  }
+}
+
 // Tile t -> (m block, n block): groups of group_m row blocks are swept
 // column by column so that CTAs running together share A and B in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
@@ -162,77 +221,131 @@ __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* a
 // Drain one 128-row x BN accumulator from tensor memory and apply the
 // epilog. Warp quarter q owns TMEM lanes 32q..32q+31 = output rows
 // row0 + 32q + lane; t_row addresses (lane 32q, first column of the buffer).
+// The drain is software-pipelined over 32-column chunks: the tensor-memory
+// load and the global side inputs (bias, mask word, saved activations) of
+// chunk c + 1 are issued before chunk c is processed, so their latencies
+// overlap its arithmetic and stores.
 // A bias-gradient epilog leaves the warp's 32-row column sums in
 // red[q * RS + column] (RS = BN unless the caller drains a wider tile in parts).
-template <int EPI, typename T, int BN, int RS = BN>
+// STG: 16-bit outputs go through this warp's 2 KB staging buffer at `stg`
+// (store_rows32_staged), else straight from registers.
+template <int EPI, typename T, int BN, int RS = BN, bool STG = false>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
-                                               int n0, int q, uint32_t lane, float* red) {
-  const int row = row0 + 32 * q + (int)lane;
+                                               int n0, int q, uint32_t lane, float* red,
+                                               uint32_t stg = 0) {
+  constexpr bool kDual = epi_dual(EPI);
+  // 16-byte side inputs per chunk: g and u (DSWIGLU), the pre-activation
+  // (DGELU_BGRAD), the column bias (bias epilogs), the mask word (DRELU_BGRAD)
+  constexpr int kSide = EPI == EPI_DSWIGLU ? 8
+                        : (EPI == EPI_DGELU_BGRAD || epi_has_bias(EPI)) ? 4
+                        : EPI == EPI_DRELU_BGRAD ? 1
+                                                 : 0;
+  constexpr int kSideN = kSide > 0 ? kSide : 1;
+  const int row0w = row0 + 32 * q;  // this warp's first row
+  const int row = row0w + (int)lane;
   const bool row_ok = row < p.M;
   const int wrow = (row0 >> 5) + q;  // relu_aux word row of this warp's 32 rows
-  const bool wrow_ok = row0 + 32 * q < p.M;
+  const bool wrow_ok = row0w < p.M;
   const T* bias = reinterpret_cast<const T*>(p.bias);
   float row_bias = 0.f;
   if constexpr (epi_has_bias(EPI)) {
     if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
   }
   T* out = reinterpret_cast<T*>(p.out);
-#pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
-    const int col0 = n0 + 32 * c;
-    if (col0 >= p.N) break;  // same for every epilogue warp
-    float v[32];
-    float u2[epi_dual(EPI) ? 32 : 1];  // the second accumulator (the SwiGLU "up" product)
-    if (p.num_k_blocks > 0) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(t_row + 32u * c, r);
-      if constexpr (epi_dual(EPI)) {
-        uint32_t r2[32];
-        tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * c, r2);
-        tmem_ld_wait();
+  const bool has_acc = p.num_k_blocks > 0;
+  const int nch = min(BN / 32, (p.N - n0 + 31) / 32);  // chunks with columns below N
+  if (nch <= 0) return;
+
+  auto load_side = [&](int col0, uint4 (&sd)[kSideN]) {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_DGELU_BGRAD) {
+      const T* ap = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) u2[j] = __uint_as_float(r2[j]);
-      } else {
-        tmem_ld_wait();
+      for (int g = 0; g < 4; ++g)
+        sd[g] = row_ok && col0 + 8 * g < p.N ? __ldg(reinterpret_cast<const uint4*>(ap + 8 * g))
+                                             : zero;
+      if constexpr (EPI == EPI_DSWIGLU) {
+        const T* up = reinterpret_cast<const T*>(p.aux_in2) + (size_t)row * p.N + col0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          sd[4 + g] = row_ok && col0 + 8 * g < p.N
+                          ? __ldg(reinterpret_cast<const uint4*>(up + 8 * g))
+                          : zero;
       }
+    } else if constexpr (EPI == EPI_DRELU_BGRAD) {
+      sd[0] = zero;
+      if (wrow_ok && col0 + (int)lane < p.N) sd[0].x = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+    } else if constexpr (epi_has_bias(EPI)) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+      for (int g = 0; g < 4; ++g)
+        sd[g] = p.bias_axis == 0 && col0 + 8 * g < p.N
+                    ? __ldg(reinterpret_cast<const uint4*>(bias + col0 + 8 * g))
+                    : zero;
+    } else {
+      sd[0] = zero;
+    }
+  };
+
+  uint32_t ra[32];
+  uint32_t rb[kDual ? 32 : 1];
+  uint4 sd[kSideN];
+  if (has_acc) {
+    tmem_ld_32x32b_x32(t_row, ra);
+    if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN, rb);
+  }
+  load_side(n0, sd);
+
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const int col0 = n0 + 32 * c;
+    float v[32];
+    float u2[kDual ? 32 : 1];  // the second accumulator (the SwiGLU "up" product)
+    if (has_acc) {
+      tmem_ld_wait_tied(ra);
+      if constexpr (kDual) tmem_tie(rb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
+      if constexpr (kDual) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u2[j] = __uint_as_float(rb[j]);
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      if constexpr (epi_dual(EPI)) {
+      if constexpr (kDual) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) u2[j] = 0.f;
       }
     }
+    uint4 cur[kSideN];
+#pragma unroll
+    for (int i = 0; i < kSideN; ++i) cur[i] = sd[i];
+    if (c + 1 < nch) {  // next chunk's loads, in flight while this one is processed
+      if (has_acc) {
+        tmem_ld_32x32b_x32(t_row + 32u * (c + 1), ra);
+        if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * (c + 1), rb);
+      }
+      load_side(col0 + 32, sd);
+    }
 
-    if constexpr (epi_dual(EPI)) {
+    if constexpr (kDual) {
       // gate+up SwiGLU: v = g = x Wg^T, u2 = u = x Wu^T; h = silu(g) * u
       if constexpr (EPI == EPI_SWIGLU_SAVE) {
-        if (row_ok) {
-          store_row32<T>(reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0, v, col0, p.N);
-          store_row32<T>(reinterpret_cast<T*>(p.aux_out2) + (size_t)row * p.N + col0, u2, col0,
-                         p.N);
-        }
+        emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, v, lane, stg);
+        emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out2), p.M, p.N, row0w, col0, u2, lane,
+                           stg);
       }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u2[j];
     } else if constexpr (EPI == EPI_DSWIGLU) {
-      // v = dh = dout Wd; saved g (aux_in) and u (aux_in2) of this row's 32
-      // columns; out = d_gate, aux_out = d_up
-      const T* gp = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
-      const T* up = reinterpret_cast<const T*>(p.aux_in2) + (size_t)row * p.N + col0;
+      // v = dh = dout Wd; saved g and u of this row's 32 columns; out = d_gate,
+      // aux_out = d_up
       float dup[32];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float g8[8], u8[8];
-        if (row_ok && col0 + 8 * g < p.N) {
-          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(gp + 8 * g)), g8);
-          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(up + 8 * g)), u8);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) g8[i] = u8[i] = 0.f;
-        }
+        unpack8<T>(cur[g], g8);
+        unpack8<T>(cur[4 + g], u8);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float s = sigmoid_f(g8[i]);
@@ -241,44 +354,28 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
           v[8 * g + i] = dh * u8[i] * s * (1.f + g8[i] * (1.f - s));
         }
       }
-      if (row_ok)
-        store_row32<T>(reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0, dup, col0, p.N);
+      emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, dup, lane, stg);
     } else if constexpr (EPI == EPI_DGELU_BGRAD) {
-      // saved pre-activation z of this row's 32 columns (T [M, N])
-      const T* zp = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
+      // saved pre-activation z of this row's 32 columns
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         float z8[8];
-        if (row_ok && col0 + 8 * g < p.N) {
-          unpack8<T>(__ldg(reinterpret_cast<const uint4*>(zp + 8 * g)), z8);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) z8[i] = 0.f;
-        }
+        unpack8<T>(cur[g], z8);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] * dgelu_tanh(z8[i]);
       }
     } else if constexpr (EPI == EPI_DRELU_BGRAD) {
-      uint32_t my_word = 0;
-      if (wrow_ok && col0 + (int)lane < p.N)
-        my_word = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+      // lane j holds the mask word of column col0 + j; transposed, lane i
+      // holds its row's bits of the 32 columns
+      const uint32_t bits = bit_transpose32(cur[0].x, lane);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t w = __shfl_sync(0xFFFFFFFFu, my_word, j);
-        v[j] = ((w >> lane) & 1u) ? v[j] : 0.f;
-      }
+      for (int j = 0; j < 32; ++j) v[j] = ((bits >> j) & 1u) ? v[j] : 0.f;
     } else if constexpr (EPI != EPI_NONE) {
       if (p.bias_axis == 0) {
-        const T* bp = bias + col0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float b8[8];
-          if (col0 + 8 * g < p.N) {
-            unpack8<T>(__ldg(reinterpret_cast<const uint4*>(bp + 8 * g)), b8);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b8[i] = 0.f;
-          }
+          unpack8<T>(cur[g], b8);
 #pragma unroll
           for (int i = 0; i < 8; ++i) v[8 * g + i] = v[8 * g + i] + b8[i];
         }
@@ -287,12 +384,12 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
         for (int j = 0; j < 32; ++j) v[j] = v[j] + row_bias;
       }
       if constexpr (EPI == EPI_RELU_AUX_BIAS) {
-        uint32_t my_word = 0;
+        // this lane's row bits (bit j: column col0 + j), transposed across the
+        // warp into column words (bit i of lane j's word: row row0w + i)
+        uint32_t bits = 0;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, row_ok && v[j] > 0.f);
-          my_word = (lane == (uint32_t)j) ? bal : my_word;
-        }
+        for (int j = 0; j < 32; ++j) bits |= (row_ok && v[j] > 0.f ? 1u : 0u) << j;
+        const uint32_t my_word = bit_transpose32(bits, lane);
         if (wrow_ok && col0 + (int)lane < p.N)
           p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
       }
@@ -302,20 +399,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
       if constexpr (EPI == EPI_GELU_AUX_BIAS) {
         // the pre-activation, rounded to T, for the backward
-        if (row_ok) {
-          T* ap = reinterpret_cast<T*>(p.aux_out) + (size_t)row * p.N + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + 8 * g < p.N) {
-              uint4 u;
-              u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
-              u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
-              u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
-              u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
-              *reinterpret_cast<uint4*>(ap + 8 * g) = u;
-            }
-          }
-        }
+        emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, v, lane, stg);
       }
       if constexpr (EPI == EPI_GELU_BIAS || EPI == EPI_GELU_AUX_BIAS) {
 #pragma unroll
@@ -323,20 +407,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     }
 
-    if (row_ok) {
-      T* op = out + (size_t)row * p.N + col0;
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        if (col0 + 8 * g < p.N) {
-          uint4 u;
-          u.x = pack2<T>(v[8 * g + 0], v[8 * g + 1]);
-          u.y = pack2<T>(v[8 * g + 2], v[8 * g + 3]);
-          u.z = pack2<T>(v[8 * g + 4], v[8 * g + 5]);
-          u.w = pack2<T>(v[8 * g + 6], v[8 * g + 7]);
-          *reinterpret_cast<uint4*>(op + 8 * g) = u;
-        }
-      }
-    }
+    emit_row32<T, STG>(out, p.M, p.N, row0w, col0, v, lane, stg);
 
     if constexpr (epi_has_bgrad(EPI)) {
       // transpose-reduce: after 5 halving steps (31 shuffles) lane l

@@ -57,9 +57,12 @@ struct PairCfg {
   static constexpr int kTmemCols = kNumAcc * kAccCols; // 512 either way
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
   static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
-  static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes);
-  static constexpr int kSmemBytes =
-      kSmemAlignSlack + kStages * (kABytes + kStageBBytes) + kCtrlBytes + kRedBytes;
+  // wide: a 2 KB output staging buffer per epilogue warp (its drain is partly
+  // exposed, so its stores go out as 64-byte row segments)
+  static constexpr int kStgBytes = WIDE ? 4 * 2048 : 0;
+  static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
+  static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
+                                    kCtrlBytes + kRedBytes + kStgBytes;
   static_assert(kStages >= 3 && kSmemBytes <= kSmemPerCta, "shared memory budget");
   static_assert(16 * kStages + 128 <= kCtrlBytes, "control region");
 };
@@ -118,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ring_s = ctrl + 16u * S + 112u;      // both: kTileRing tile indices
   volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
+  const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // wide: 4 x 2 KB staging
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -422,11 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
         // half 0, release it (the next tile's first MMAs go there), half 1
-        epilogue_drain<EPI, T, 256, BN>(p, t_row, row0, n0, q, lane, red);
+        const uint32_t stg = stg0 + 2048u * (uint32_t)q;
+        epilogue_drain<EPI, T, 256, BN, true>(p, t_row, row0, n0, q, lane, red, stg);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader);
-        epilogue_drain<EPI, T, 256, BN>(p, t_row + 256u, row0, n0 + 256, q, lane, red + 256);
+        epilogue_drain<EPI, T, 256, BN, true>(p, t_row + 256u, row0, n0 + 256, q, lane, red + 256,
+                                              stg);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
