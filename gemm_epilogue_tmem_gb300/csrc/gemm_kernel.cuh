@@ -218,6 +218,39 @@ __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* a
   atomicOr(p.status, code);
 }
 
+// Per-tile side inputs of a drain, fetched into this warp's shared buffer at
+// `side` before the accumulator is ready (the loads overlap the mainloop):
+// the column bias of columns n0 .. n0 + NC - 1 (T, zero past N; bias epilogs
+// with a per-column bias), or the mask words of this warp's 32 rows for the
+// same columns (uint32, zero past N or M; DRELU_BGRAD). Called by all 32 lanes.
+template <int EPI, typename T, int NC>
+__device__ __forceinline__ void prefetch_side(const GemmParams& p, int row0w, int n0,
+                                              uint32_t lane, uint32_t side) {
+  if constexpr (EPI == EPI_DRELU_BGRAD) {
+    const int wrow = row0w >> 5;
+    const bool wrow_ok = row0w < p.M;
+#pragma unroll
+    for (int i = 0; i < NC / 32; ++i) {
+      const int col = n0 + 32 * i + (int)lane;
+      const uint32_t w = wrow_ok && col < p.N ? __ldg(p.aux_in + (size_t)wrow * p.N + col) : 0u;
+      st_shared_u32(side + 4u * (uint32_t)(32 * i + (int)lane), w);
+    }
+  } else if constexpr (epi_has_bias(EPI)) {
+    if (p.bias_axis == 0) {
+      const T* bias = reinterpret_cast<const T*>(p.bias);
+      // NC columns of 2 bytes: 16-byte pieces, lane-strided
+#pragma unroll
+      for (int i = 0; i < NC / 256; ++i) {
+        const int col = n0 + 8 * (32 * i + (int)lane);
+        const uint4 b = col < p.N ? __ldg(reinterpret_cast<const uint4*>(bias + col))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(side + 16u * (uint32_t)(32 * i + (int)lane), b.x, b.y, b.z, b.w);
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // Drain one 128-row x BN accumulator from tensor memory and apply the
 // epilog. Warp quarter q owns TMEM lanes 32q..32q+31 = output rows
 // row0 + 32q + lane; t_row addresses (lane 32q, first column of the buffer).
@@ -228,11 +261,13 @@ __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* a
 // A bias-gradient epilog leaves the warp's 32-row column sums in
 // red[q * RS + column] (RS = BN unless the caller drains a wider tile in parts).
 // STG: 16-bit outputs go through this warp's 2 KB staging buffer at `stg`
-// (store_rows32_staged), else straight from registers.
-template <int EPI, typename T, int BN, int RS = BN, bool STG = false>
+// (store_rows32_staged), else straight from registers. SIDE: the column bias
+// (T) or this warp's mask words (uint32) of columns n0.. were prefetched into
+// shared memory at `side` (prefetch_side), and are read from there.
+template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red,
-                                               uint32_t stg = 0) {
+                                               uint32_t stg = 0, uint32_t side = 0) {
   constexpr bool kDual = epi_dual(EPI);
   // 16-byte side inputs per chunk: g and u (DSWIGLU), the pre-activation
   // (DGELU_BGRAD), the column bias (bias epilogs), the mask word (DRELU_BGRAD)
@@ -274,13 +309,22 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     } else if constexpr (EPI == EPI_DRELU_BGRAD) {
       sd[0] = zero;
-      if (wrow_ok && col0 + (int)lane < p.N) sd[0].x = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+      if constexpr (SIDE) {
+        sd[0].x = ld_shared_u32(side + 4u * (uint32_t)(col0 - n0 + (int)lane));
+      } else if (wrow_ok && col0 + (int)lane < p.N) {
+        sd[0].x = __ldg(p.aux_in + (size_t)wrow * p.N + col0 + lane);
+      }
     } else if constexpr (epi_has_bias(EPI)) {
+      if constexpr (SIDE) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        sd[g] = p.bias_axis == 0 && col0 + 8 * g < p.N
-                    ? __ldg(reinterpret_cast<const uint4*>(bias + col0 + 8 * g))
-                    : zero;
+        for (int g = 0; g < 4; ++g) sd[g] = ld_shared_v4(side + 2u * (uint32_t)(col0 - n0) + 16u * g);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          sd[g] = p.bias_axis == 0 && col0 + 8 * g < p.N
+                      ? __ldg(reinterpret_cast<const uint4*>(bias + col0 + 8 * g))
+                      : zero;
+      }
     } else {
       sd[0] = zero;
     }

@@ -57,9 +57,10 @@ struct PairCfg {
   static constexpr int kTmemCols = kNumAcc * kAccCols; // 512 either way
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
   static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
-  // wide: a 2 KB output staging buffer per epilogue warp (its drain is partly
-  // exposed, so its stores go out as 64-byte row segments)
-  static constexpr int kStgBytes = WIDE ? 4 * 2048 : 0;
+  // wide: per epilogue warp a 2 KB output staging buffer (its drain is partly
+  // exposed, so its stores go out as 64-byte row segments) and a 2 KB buffer
+  // of the tile's prefetched side inputs (column bias or mask words)
+  static constexpr int kStgBytes = WIDE ? 4 * (2048 + 2048) : 0;
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes + kStgBytes;
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
   const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // wide: 4 x 2 KB staging
+  const uint32_t side0 = stg0 + 4u * 2048u;                     // wide: 4 x 2 KB side inputs
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -408,6 +410,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (t < 0) break;
+      int mb2, nb;
+      pair_tile_coords(p, t, mb2, nb);
+      const int row0 = mb2 * 256 + 128 * (int)rank;
+      const int n0 = nb * BN;
+      constexpr bool kSide = WIDE && (EPI == EPI_DRELU_BGRAD || epi_has_bias(EPI));
+      const uint32_t side = side0 + 2048u * (uint32_t)q;
+      if constexpr (kSide) prefetch_side<EPI, T, BN>(p, row0 + 32 * q, n0, lane, side);
       const int buf = WIDE ? 0 : (it & 1);
       const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
       ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
@@ -418,21 +427,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      int mb2, nb;
-      pair_tile_coords(p, t, mb2, nb);
-      const int row0 = mb2 * 256 + 128 * (int)rank;
-      const int n0 = nb * BN;
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
         // half 0, release it (the next tile's first MMAs go there), half 1
         const uint32_t stg = stg0 + 2048u * (uint32_t)q;
-        epilogue_drain<EPI, T, 256, BN, true>(p, t_row, row0, n0, q, lane, red, stg);
+        // side inputs of half 1 start 256 columns in: 512 bytes of bias or 1 KB of words
+        constexpr uint32_t kSideHalf = EPI == EPI_DRELU_BGRAD ? 1024u : 512u;
+        epilogue_drain<EPI, T, 256, BN, true, kSide>(p, t_row, row0, n0, q, lane, red, stg, side);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader);
-        epilogue_drain<EPI, T, 256, BN, true>(p, t_row + 256u, row0, n0 + 256, q, lane, red + 256,
-                                              stg);
+        epilogue_drain<EPI, T, 256, BN, true, kSide>(p, t_row + 256u, row0, n0 + 256, q, lane,
+                                                     red + 256, stg, side + kSideHalf);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
