@@ -35,7 +35,7 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
@@ -58,7 +58,7 @@ int pair_max_clusters() {
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -240,11 +240,11 @@ __device__ __forceinline__ void prefetch_side(const GemmParams& p, int row0w, in
       const T* bias = reinterpret_cast<const T*>(p.bias);
       // NC columns of 2 bytes: 16-byte pieces, lane-strided
 #pragma unroll
-      for (int i = 0; i < NC / 256; ++i) {
-        const int col = n0 + 8 * (32 * i + (int)lane);
+      for (int pc = (int)lane; pc < NC / 8; pc += 32) {
+        const int col = n0 + 8 * pc;
         const uint4 b = col < p.N ? __ldg(reinterpret_cast<const uint4*>(bias + col))
                                   : make_uint4(0u, 0u, 0u, 0u);
-        st_shared_v4(side + 16u * (uint32_t)(32 * i + (int)lane), b.x, b.y, b.z, b.w);
+        st_shared_v4(side + 16u * (uint32_t)pc, b.x, b.y, b.z, b.w);
       }
     }
   }
@@ -473,13 +473,13 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
 
 // Column sums of the tile's 128 rows: the four warps' 32-row sums (in red,
 // [4][BN]) added in a fixed order, then one partial per 128-row block or one
-// atomicAdd per column. Called by the 128 epilogue threads (ep_tid 0..127).
-template <int BN>
+// atomicAdd per column. Called by the NT epilogue threads (ep_tid 0..NT-1).
+template <int BN, int NT = 128>
 __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float* red, int ep_tid,
                                                int n0, int mb) {
-  if (mb >= p.num_m_blocks) return;  // rows past M (same for all 128 threads): nothing to add
-  named_bar_sync(1, 128);
-  for (int col = ep_tid; col < BN; col += 128) {
+  if (mb >= p.num_m_blocks) return;  // rows past M (same for all NT threads): nothing to add
+  named_bar_sync(1, NT);
+  for (int col = ep_tid; col < BN; col += NT) {
     if (n0 + col < p.N) {
       // the four warps' 32-row sums, always in the same order
       const float s = ((red[col] + red[BN + col]) + red[2 * BN + col]) + red[3 * BN + col];
@@ -489,7 +489,7 @@ __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float*
         p.bgrad[(size_t)mb * p.N + n0 + col] = s;
     }
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(1, NT);
 }
 
 template <int EPI, typename T, bool B_MN, int BN>

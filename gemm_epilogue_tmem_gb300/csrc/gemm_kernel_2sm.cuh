@@ -55,12 +55,19 @@ struct PairCfg {
   static constexpr int kAccCols = WIDE ? 512 : 256;    // TMEM columns of one accumulator
   static constexpr int kNumAcc = WIDE ? 1 : 2;         // accumulator buffers
   static constexpr int kTmemCols = kNumAcc * kAccCols; // 512 either way
+  // epilogue warps: wide tiles drain with two warps per TMEM lane quarter
+  // (each takes half of the columns), so that their exposed drain is short
+  static constexpr int kEpiWarps = WIDE ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // consumers of a tile index: leader MMA + peer producer + both CTAs' epilogue warps
+  static constexpr int kTileConsumers = 2 + 2 * kEpiWarps;
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
   static constexpr int kRedBytes = RED ? 4 * BN * 4 : 0;
   // wide: per epilogue warp a 2 KB output staging buffer (its drain is partly
-  // exposed, so its stores go out as 64-byte row segments) and a 2 KB buffer
-  // of the tile's prefetched side inputs (column bias or mask words)
-  static constexpr int kStgBytes = WIDE ? 4 * (2048 + 2048) : 0;
+  // exposed, so its stores go out as 64-byte row segments) and a 1 KB buffer
+  // of the tile's prefetched side inputs (column bias or mask words of its
+  // 2 x 128 columns)
+  static constexpr int kStgBytes = WIDE ? kEpiWarps * (2048 + 1024) : 0;
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes + kStgBytes;
@@ -69,8 +76,6 @@ struct PairCfg {
 };
 
 constexpr int kTileRing = 4;  // tile indices in flight between the roles (dynamic schedule)
-// consumers of a tile index: leader MMA + 4 epilogue warps, peer producer + 4 epilogue warps
-constexpr int kTileConsumers = 10;
 
 // Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
 __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int& mb2, int& nb) {
@@ -89,7 +94,7 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 }
 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kThreads, 1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
   const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // wide: 4 x 2 KB staging
-  const uint32_t side0 = stg0 + 4u * 2048u;                     // wide: 4 x 2 KB side inputs
+  const uint32_t side0 = stg0 + C::kEpiWarps * 2048u;           // wide: 1 KB side inputs per warp
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
@@ -141,12 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(tfull0, 1);
     mbar_init(tfull0 + 8u, 1);
-    mbar_init(tempty0, 8);
-    mbar_init(tempty0 + 8u, 8);
+    mbar_init(tempty0, 2 * C::kEpiWarps);
+    mbar_init(tempty0 + 8u, 2 * C::kEpiWarps);
     mbar_init(done_bar, 1);
     for (int r = 0; r < kTileRing; ++r) {
       mbar_init(tile_full0 + 8u * r, 1);
-      mbar_init(tile_empty0 + 8u * r, kTileConsumers);
+      mbar_init(tile_empty0 + 8u * r, C::kTileConsumers);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -392,7 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
+    // warp w drains TMEM lanes 32 (w % 4)..; with 8 epilogue warps (wide) the
+    // two warps of a lane quarter take column halves `sub` 0 and 1
+    constexpr int NT = 32 * C::kEpiWarps;  // epilogue threads
     const int q = warp & 3;
+    const int sub = (warp - 2) >> 2;
     const int ep_tid = threadIdx.x - 64;
     const uint32_t tempty_leader = mapa_shared(tempty0, 0);
     for (int it = 0;; ++it) {
@@ -403,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_remote(tile_empty_leader + 8u * (it % kTileRing));
       }
       bool ok = t != -2;
-      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
+      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, NT, !ok);
       if (!ok) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
         aborted = true;
@@ -414,13 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       pair_tile_coords(p, t, mb2, nb);
       const int row0 = mb2 * 256 + 128 * (int)rank;
       const int n0 = nb * BN;
+      // wide: this warp's 128 columns of each accumulator half, their side
+      // inputs (bias or mask words) prefetched while the mainloop runs
       constexpr bool kSide = WIDE && (EPI == EPI_DRELU_BGRAD || epi_has_bias(EPI));
-      const uint32_t side = side0 + 2048u * (uint32_t)q;
-      if constexpr (kSide) prefetch_side<EPI, T, BN>(p, row0 + 32 * q, n0, lane, side);
+      constexpr uint32_t kSideHalf = EPI == EPI_DRELU_BGRAD ? 512u : 256u;  // 128 columns
+      const int c_sub = 128 * sub;
+      const uint32_t side = side0 + 1024u * (uint32_t)(warp - 2);
+      if constexpr (kSide) {
+        prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + c_sub, lane, side);
+        prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + 256 + c_sub, lane, side + kSideHalf);
+      }
       const int buf = WIDE ? 0 : (it & 1);
       const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
       ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
-      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, 128, !ok);
+      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, NT, !ok);
       if (!ok) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
         aborted = true;
@@ -431,15 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
         // half 0, release it (the next tile's first MMAs go there), half 1
-        const uint32_t stg = stg0 + 2048u * (uint32_t)q;
-        // side inputs of half 1 start 256 columns in: 512 bytes of bias or 1 KB of words
-        constexpr uint32_t kSideHalf = EPI == EPI_DRELU_BGRAD ? 1024u : 512u;
-        epilogue_drain<EPI, T, 256, BN, true, kSide>(p, t_row, row0, n0, q, lane, red, stg, side);
+        const uint32_t stg = stg0 + 2048u * (uint32_t)(warp - 2);
+        epilogue_drain<EPI, T, 128, BN, true, kSide>(p, t_row + (uint32_t)c_sub, row0, n0 + c_sub,
+                                                     q, lane, red + c_sub, stg, side);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader);
-        epilogue_drain<EPI, T, 256, BN, true, kSide>(p, t_row + 256u, row0, n0 + 256, q, lane,
-                                                     red + 256, stg, side + kSideHalf);
+        epilogue_drain<EPI, T, 128, BN, true, kSide>(p, t_row + 256u + (uint32_t)c_sub, row0,
+                                                     n0 + 256 + c_sub, q, lane,
+                                                     red + 256 + c_sub, stg, side + kSideHalf);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
@@ -449,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       }
-      if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN>(p, red, ep_tid, n0, row0 / kBM);
+      if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN, NT>(p, red, ep_tid, n0, row0 / kBM);
     }
   }
 

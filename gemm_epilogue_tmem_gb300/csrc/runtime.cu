@@ -157,18 +157,27 @@ void plan_tiles(gf_plan* p) {
   // with two B operands) moves 2/3 of the operand bytes per flop of the
   // single-CTA tile; take it when its tiles fill the resident pairs, else the
   // single-CTA kernel with the tile width that keeps the SMs busy.
-  // Wide pair tiles (256 x 512, forced_kernel 3) need 3/4 of the operand
-  // bytes per flop of the 256 x 256 pair tile but expose part of each
-  // epilogue; one B operand only.
-  const bool wide = p->forced_kernel == 3 && !dual && p->max_pair_clusters > 0;
+  // Wide pair tiles (256 x 512) need 3/4 of the operand bytes per flop of
+  // the 256 x 256 pair tile but expose part of each epilogue (a few thousand
+  // cycles per tile): the plan takes them when a tile's mainloop is long
+  // (k >= 8192) and their coarser waves cost no more than 3 % of the
+  // 256 x 256 schedule; one B operand only.
+  const int64_t m2 = (p->m + 255) / 256;
+  const int64_t tiles256 = m2 * ((p->n + (dual ? 127 : 255)) / (dual ? 128 : 256));
+  const int64_t tiles512 = m2 * ((p->n + 511) / 512);
+  const int64_t cl = p->max_pair_clusters > 0 ? p->max_pair_clusters : 1;
+  const bool wide_fits = !dual && p->max_pair_clusters > 0;
+  const bool wide_pays = wide_fits && p->k >= 8192 &&
+                         100 * 2 * ((tiles512 + cl - 1) / cl) <= 103 * ((tiles256 + cl - 1) / cl);
+  const bool wide = wide_fits && (p->forced_kernel == 3 || (p->forced_kernel == 0 && wide_pays));
   const int pair_n = wide ? 512 : (dual ? 128 : 256);
-  const int64_t pair_tiles = ((p->m + 255) / 256) * ((p->n + pair_n - 1) / pair_n);
+  const int64_t pair_tiles = wide ? tiles512 : tiles256;
   bool pair = false;
   if (p->forced_kernel == 2 || p->forced_kernel == 3)
     pair = p->max_pair_clusters > 0;
   else if (p->forced_kernel == 0)
     pair = p->max_pair_clusters > 0 && p->forced_tile_n == 0 && p->m > 128 &&
-           pair_tiles >= p->max_pair_clusters;
+           tiles256 >= p->max_pair_clusters;
   p->pair = pair ? 1 : 0;
   p->wide = pair && wide ? 1 : 0;
   if (pair) {

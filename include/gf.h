@@ -226,7 +226,11 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          stage load, so the consumer's bounded wait runs
  *                          out; execute then completes with
  *                          GF_ERR_DEVICE_TIMEOUT from gf_plan_status. 0: off.
- * GF_OPT_KERNEL          : 0 the plan's choice, 1 the single-CTA kernel
+ * GF_OPT_KERNEL          : 0 the plan's choice (the CTA-pair kernel when its
+ *                          256-row tiles fill the resident pairs, with
+ *                          256 x 512 tiles when k >= 8192 and their waves
+ *                          quantise no worse; else the single-CTA kernel),
+ *                          1 the single-CTA kernel
  *                          (128 x tile_n tiles), 2 the CTA-pair kernel
  *                          (256 x 256 tiles on two SMs; GF_ERR_UNSUPPORTED if
  *                          it cannot be resident on this device), 3 the
