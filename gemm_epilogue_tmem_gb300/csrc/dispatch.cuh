@@ -25,7 +25,8 @@ cudaError_t launch_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE>;
-  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kSmemBytes;
+  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>;
+  constexpr int smem = C::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e =
@@ -35,7 +36,7 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.grid, 1, 1);
-  cfg.blockDim = dim3(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
@@ -52,13 +53,14 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN>
 int pair_max_clusters() {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  constexpr int smem = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kSmemBytes;
+  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), false, pair_epi8(EPI, false)>;
+  constexpr int smem = C::kSmemBytes;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI)>::kThreads, 1, 1);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

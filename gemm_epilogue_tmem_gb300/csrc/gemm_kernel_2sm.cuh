@@ -40,10 +40,17 @@
 
 namespace gf {
 
+// Eight epilogue warps (two per TMEM lane quarter) for the wide tiles, whose
+// drain is partly exposed. (The 256 x 256 tiles' drain runs under the next
+// mainloop; their epilogues that read 16-bit side inputs per element ran
+// slower with eight warps than with four.)
+GF_HD constexpr bool pair_epi8(int epi, bool wide) { return wide && epi >= 0; }
+
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
 // side in one accumulator); RED = the epilog reduces a bias gradient and
-// needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only).
-template <int NB = 1, bool RED = false, bool WIDE = false>
+// needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only); EPI8 =
+// eight epilogue warps (pair_epi8).
+template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE>
 struct PairCfg {
   static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
   static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
@@ -55,9 +62,9 @@ struct PairCfg {
   static constexpr int kAccCols = WIDE ? 512 : 256;    // TMEM columns of one accumulator
   static constexpr int kNumAcc = WIDE ? 1 : 2;         // accumulator buffers
   static constexpr int kTmemCols = kNumAcc * kAccCols; // 512 either way
-  // epilogue warps: wide tiles drain with two warps per TMEM lane quarter
-  // (each takes half of the columns), so that their exposed drain is short
-  static constexpr int kEpiWarps = WIDE ? 8 : 4;
+  // epilogue warps: EPI8 drains with two warps per TMEM lane quarter (each
+  // takes half of the columns)
+  static constexpr int kEpiWarps = EPI8 ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   // consumers of a tile index: leader MMA + peer producer + both CTAs' epilogue warps
   static constexpr int kTileConsumers = 2 + 2 * kEpiWarps;
@@ -94,12 +101,13 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 }
 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
-__global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE>::kThreads, 1)
+__global__ void __launch_bounds__(
+    PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>::kThreads, 1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE>;
+  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -318,6 +326,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             break;
           }
           umma_commit_pair(tfull0 + 8u * buf, 0x3);  // nothing to multiply: acc is zero
+          if (WIDE) umma_commit_pair(tfull0 + 8u, 0x3);
           continue;
         }
         // the MMAs of one k-slice into accumulator half h (wide) or the whole
@@ -372,7 +381,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           }
           kb = pre;
         }
-        for (; kb < p.num_k_blocks; ++kb) {
+        // wide: the last S k-slices go half 0 first, then half 1, so that
+        // half 0 is complete (and its drain starts) S k-slices early
+        const int tail = WIDE && p.num_k_blocks - kb >= 2 * S ? S : 0;
+        for (; kb < p.num_k_blocks - tail; ++kb) {
           if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
             ok = false;
@@ -388,7 +400,42 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit_pair(tfull0 + 8u * buf, 0x3);
+        if (!ok) break;
+        if constexpr (WIDE) {
+          if (tail > 0) {
+            int st = stage;
+            uint32_t ph = phase;
+            for (int j = 0; j < tail; ++j) {
+              if (!mbar_wait_bounded(full0 + 8u * st, ph, abort_flag, p.wait_limit_ns)) {
+                raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
+                ok = false;
+                aborted = true;
+                break;
+              }
+              tc_fence_after();
+              mma_kslice(st, kb + j, 0);
+              if (++st == S) {
+                st = 0;
+                ph ^= 1u;
+              }
+            }
+            if (!ok) break;
+            umma_commit_pair(tfull0, 0x3);  // half 0 complete
+            for (int j = 0; j < tail; ++j) {
+              mma_kslice(stage, kb + j, 1);
+              umma_commit_pair(empty0 + 8u * stage, 0x3);
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          } else {
+            umma_commit_pair(tfull0, 0x3);
+          }
+          umma_commit_pair(tfull0 + 8u, 0x3);  // half 1 complete
+        } else {
+          umma_commit_pair(tfull0 + 8u * buf, 0x3);
+        }
       }
       umma_commit_pair(done_bar, 0x1);
       if (!mbar_wait_bounded(done_bar, 0, nullptr, p.wait_limit_ns))
@@ -453,12 +500,29 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader);
+        // half 1 is complete a few k-slices after half 0
+        bool ok1 = mbar_wait_bounded(tfull0 + 8u, use, abort_flag, p.wait_limit_ns);
+        if constexpr (epi_has_bgrad(EPI)) ok1 = !named_bar_red_or(1, NT, !ok1);
+        if (!ok1) {
+          raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
         epilogue_drain<EPI, T, 128, BN, true, kSide>(p, t_row + 256u + (uint32_t)c_sub, row0,
                                                      n0 + 256 + c_sub, q, lane,
                                                      red + 256 + c_sub, stg, side + kSideHalf);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
+      } else if constexpr (C::kEpiWarps == 8) {
+        // this warp's half of the tile's columns
+        constexpr int H = BN / 2;
+        epilogue_drain<EPI, T, H, BN>(p, t_row + (uint32_t)(H * sub), row0, n0 + H * sub, q, lane,
+                                      red + H * sub);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       } else {
         epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
         tc_fence_before();
