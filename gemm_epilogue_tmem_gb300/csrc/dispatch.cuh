@@ -25,7 +25,8 @@ cudaError_t launch_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE>;
-  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>;
+  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE),
+                    pair_stg(EPI, WIDE)>;
   constexpr int smem = C::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
@@ -53,7 +54,8 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
 template <int EPI, typename T, bool B_MN>
 int pair_max_clusters() {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN>;
-  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), false, pair_epi8(EPI, false)>;
+  using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), false, pair_epi8(EPI, false),
+                    pair_stg(EPI, false)>;
   constexpr int smem = C::kSmemBytes;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)

@@ -46,11 +46,18 @@ namespace gf {
 // slower with eight warps than with four.)
 GF_HD constexpr bool pair_epi8(int epi, bool wide) { return wide && epi >= 0; }
 
+// Output staging through shared memory (64-byte row segments): the wide
+// tiles, and on 256 x 256 tiles the epilogs that store two or three 16-bit
+// outputs per element (one ring stage makes room for it).
+GF_HD constexpr bool pair_stg(int epi, bool wide) {
+  return wide || epi == EPI_GELU_AUX_BIAS || epi == EPI_SWIGLU_SAVE || epi == EPI_DSWIGLU;
+}
+
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
 // side in one accumulator); RED = the epilog reduces a bias gradient and
 // needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only); EPI8 =
 // eight epilogue warps (pair_epi8).
-template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE>
+template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE, bool STG = WIDE>
 struct PairCfg {
   static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
   static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
@@ -74,7 +81,7 @@ struct PairCfg {
   // exposed, so its stores go out as 64-byte row segments) and a 1 KB buffer
   // of the tile's prefetched side inputs (column bias or mask words of its
   // 2 x 128 columns)
-  static constexpr int kStgBytes = WIDE ? kEpiWarps * (2048 + 1024) : 0;
+  static constexpr int kStgBytes = WIDE ? kEpiWarps * (2048 + 1024) : (STG ? kEpiWarps * 2048 : 0);
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes + kStgBytes;
@@ -101,13 +108,14 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 }
 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
-__global__ void __launch_bounds__(
-    PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>::kThreads, 1)
+__global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
+                                          pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE)>::kThreads,
+                                  1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE)>;
+  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE)>;
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -135,7 +143,7 @@ __global__ void __launch_bounds__(
   const uint32_t ring_s = ctrl + 16u * S + 112u;      // both: kTileRing tile indices
   volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
-  const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // wide: 4 x 2 KB staging
+  const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // 2 KB output staging per warp
   const uint32_t side0 = stg0 + C::kEpiWarps * 2048u;           // wide: 1 KB side inputs per warp
 
   const int warp = threadIdx.x >> 5;
@@ -524,7 +532,9 @@ __global__ void __launch_bounds__(
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       } else {
-        epilogue_drain<EPI, T, BN>(p, t_row, row0, n0, q, lane, red);
+        constexpr bool kStg = pair_stg(EPI, false);
+        epilogue_drain<EPI, T, BN, BN, kStg>(p, t_row, row0, n0, q, lane, red,
+                                             stg0 + 2048u * (uint32_t)(warp - 2));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);

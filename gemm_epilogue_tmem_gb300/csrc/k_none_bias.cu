@@ -9,6 +9,12 @@ cudaError_t launch_none_bias(int epi, const LaunchArgs& a) {
 
 int stages_for(int tile_n, int pair, int epi) {
   const bool red = epi_has_bgrad(epi);
+  if (epi_dual(epi) && pair)
+    return pair_stg(epi, false) ? PairCfg<2, false, false, false, true>::kStages
+                                : PairCfg<2, false>::kStages;
+  if (pair && tile_n != 512 && pair_stg(epi, false))
+    return red ? PairCfg<1, true, false, false, true>::kStages
+               : PairCfg<1, false, false, false, true>::kStages;
   if (epi_dual(epi))
     return pair ? (red ? PairCfg<2, true>::kStages : PairCfg<2, false>::kStages)
                 : (red ? TileCfg<128, 2, true>::kStages : TileCfg<128, 2, false>::kStages);
