@@ -754,6 +754,71 @@ def run_swiglu_workload(args, gf, torch, dev, sp, peak, pk, Ms):
     return out
 
 
+def run_small_workloads(args, gf, torch, dev, sp, peak, pk):
+    """The pages' two small workloads, latency-bound (reported, not held to a
+    peak fraction): the tiny 2-layer ReLU MLP step (layer-1 forward
+    RELU_AUX_BIAS 256x384x512 + backward DRELU_BGRAD G = dY W2^T 256x384x128)
+    and the row-bias RELU_BIAS GEMM 1024x512x2048; per launch, L2 warm
+    (the inputs fit in L2), against the same work unfused in torch."""
+    out = []
+    f16 = torch.float16
+    # MLP step
+    rc = synth.MLP_TINY
+    X, W1, b1, W2, dY = (_dev_fill(torch, rc, n, dev, sp) for n in ("X", "W1", "b1", "W2", "dY"))
+    Mx, Kx = rc.tensors["X"].shape
+    Nh = rc.tensors["W1"].shape[1]
+    No = rc.tensors["W2"].shape[1]
+    Y = torch.empty((Mx, Nh), dtype=f16, device=dev)
+    aux = torch.empty(((Mx + 31) // 32, Nh), dtype=torch.int32, device=dev)
+    G = torch.empty((Mx, Nh), dtype=f16, device=dev)
+    bg = torch.empty((Nh,), dtype=torch.float32, device=dev)
+    fwd = gf.gf_matmul_plan(Mx, Nh, Kx, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    bwd = gf.gf_matmul_plan_ex(Mx, Nh, No, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                               gf.GF_B_NK)
+
+    def fused_step():
+        gf.gf_matmul_execute(fwd, X, W1, bias=b1, out=Y, aux_out=aux, stream=sp)
+        gf.gf_matmul_execute(bwd, dY, W2, out=G, aux_in=aux, bgrad=bg, stream=sp)
+
+    def torch_step():
+        z = torch.addmm(b1, X, W1)
+        y = torch.relu(z)
+        m = z > 0
+        g = torch.matmul(dY, W2.t()) * m
+        return y, g.float().sum(0)
+
+    ms = _interleaved(torch, {"fused": fused_step, "torch_unfused": torch_step}, reps=200)
+    flop = 2.0 * Mx * Nh * Kx + 2.0 * Mx * Nh * No
+    ok = gf.gf_plan_status(fwd, sp) == gf.GF_OK and gf.gf_plan_status(bwd, sp) == gf.GF_OK
+    out.append({"workload": f"mlp2_relu_fp16_fwd_{Mx}x{Nh}x{Kx}_bwd_{Mx}x{Nh}x{No}",
+                "value": flop / (ms["fused"] * 1e-3) / 1e12, "ms_per_step": ms["fused"],
+                "us_per_step": 1e3 * ms["fused"], "torch_unfused_us": 1e3 * ms["torch_unfused"],
+                "fused_vs_torch_unfused": ms["torch_unfused"] / ms["fused"], "launches_per_step": 3,
+                "l2": "inputs fit in L2 (latency-bound)", "status_ok": ok})
+    fwd.free()
+    bwd.free()
+    # row-bias RELU_BIAS
+    rc = synth.RELU_BIAS_ROW
+    A, B, bias = (_dev_fill(torch, rc, n, dev, sp) for n in ("A", "B", "bias"))
+    Mr, Kr = rc.tensors["A"].shape
+    Nr = rc.tensors["B"].shape[1]
+    Yr = torch.empty((Mr, Nr), dtype=f16, device=dev)
+    plan = gf.gf_matmul_plan(Mr, Nr, Kr, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_ROW)
+    ms = _interleaved(torch, {
+        "fused": lambda: gf.gf_matmul_execute(plan, A, B, bias=bias, out=Yr, stream=sp),
+        "torch_unfused": lambda: torch.relu(torch.addmm(bias[:, None], A, B)),
+    }, reps=200)
+    flop = 2.0 * Mr * Nr * Kr
+    out.append({"workload": f"relu_bias_rowbias_fp16_{Mr}x{Nr}x{Kr}",
+                "value": flop / (ms["fused"] * 1e-3) / 1e12, "ms_per_step": ms["fused"],
+                "us_per_step": 1e3 * ms["fused"], "torch_unfused_us": 1e3 * ms["torch_unfused"],
+                "fused_vs_torch_unfused": ms["torch_unfused"] / ms["fused"], "launches_per_step": 1,
+                "plan": gf.gf_plan_describe(plan), "l2": "inputs fit in L2 (latency-bound)",
+                "status_ok": gf.gf_plan_status(plan, sp) == gf.GF_OK})
+    plan.free()
+    return out
+
+
 def run_workload(args):
     """`--workload gelu|swiglu`: the pages' other two workloads, one JSON line
     each, with the fused kernels' throughput, the epilogue overhead against a
@@ -772,11 +837,14 @@ def run_workload(args):
     pk = f"{kind} {key}"
     if args.workload == "gelu":
         lines = [run_gelu_workload(args, gf, torch, dev, sp, peak, pk)]
+    elif args.workload == "small":
+        lines = run_small_workloads(args, gf, torch, dev, sp, peak, pk)
     else:
         Ms = [int(v) for v in args.swiglu_m.split(",")]
         lines = run_swiglu_workload(args, gf, torch, dev, sp, peak, pk, Ms)
     for ln in lines:
-        print(json.dumps({"metric": METRIC, "unit": "TFLOP/s", "dtype": "bf16",
+        print(json.dumps({"metric": METRIC, "unit": "TFLOP/s",
+                          "dtype": "f16" if args.workload == "small" else "bf16",
                           "data": "synthetic", "higher_is_better": True, **ln}), flush=True)
     return 0 if all(ln["status_ok"] for ln in lines) else 1
 
@@ -874,8 +942,9 @@ def main():
     ap.add_argument("--autotune", action="store_true",
                     help="let gf_matmul_autotune pick the kernels before the warm-up")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="linear_pair", choices=["linear_pair", "gelu", "swiglu"],
-                    help="gelu / swiglu: the other two workloads, one JSON line each")
+    ap.add_argument("--workload", default="linear_pair",
+                    choices=["linear_pair", "gelu", "swiglu", "small"],
+                    help="gelu / swiglu / small: the other workloads, one JSON line each")
     ap.add_argument("--swiglu-m", default="2048,8192,16384")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "gf":

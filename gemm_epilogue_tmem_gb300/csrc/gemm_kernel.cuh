@@ -430,9 +430,11 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       if constexpr (EPI == EPI_RELU_AUX_BIAS) {
         // this lane's row bits (bit j: column col0 + j), transposed across the
         // warp into column words (bit i of lane j's word: row row0w + i)
-        uint32_t bits = 0;
+        // four independent OR chains (a short dependency path), then merged
+        uint32_t b4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) bits |= (row_ok && v[j] > 0.f ? 1u : 0u) << j;
+        for (int j = 0; j < 32; ++j) b4[j & 3] |= (v[j] > 0.f ? 1u : 0u) << j;
+        const uint32_t bits = row_ok ? (b4[0] | b4[1]) | (b4[2] | b4[3]) : 0u;
         const uint32_t my_word = bit_transpose32(bits, lane);
         if (wrow_ok && col0 + (int)lane < p.N)
           p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
