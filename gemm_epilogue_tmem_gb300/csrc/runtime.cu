@@ -281,8 +281,17 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
   p->b_layout = b_layout;
   p->device = dev;
   p->num_sms = prop.multiProcessorCount;
+  // defaults, and the environment overrides of experiments (an option set
+  // on the plan afterwards wins)
   p->bgrad_mode = GF_BGRAD_TWO_PASS;
+  const char* env_bgrad = getenv("GF_BGRAD_MODE");
+  if (env_bgrad && strcmp(env_bgrad, "atomic") == 0) p->bgrad_mode = GF_BGRAD_ATOMIC;
   p->wait_limit_ns = 2000000000ull;
+  const char* env_wait = getenv("GF_WAIT_LIMIT_US");
+  if (env_wait) {
+    const long long us = atoll(env_wait);
+    if (us >= 1000 && us <= 600000000) p->wait_limit_ns = static_cast<uint64_t>(us) * 1000ull;
+  }
   const char* env_tile = getenv("GF_TILE_N");
   p->forced_tile_n = env_tile && (atoi(env_tile) == 128 || atoi(env_tile) == 256) ? atoi(env_tile) : 0;
   const char* env_kernel = getenv("GF_KERNEL");
