@@ -1,9 +1,11 @@
 """The CTA-pair kernel with 256 x 512 tiles (GF_OPT_KERNEL = 3): one
 512-column accumulator per pair, drained in two halves while the next tile
-starts on the first half. Checked against the oracle on ragged shapes (N not a
-multiple of 512 or of 64, K not a multiple of 64, fewer k-slices than ring
-stages, K = 0), on every epilog family it serves, with many tiles per CTA
-pair, under both schedules, and through a bounded wait that runs out."""
+starts on the first half and the last k-slices of a tile finish the first
+half early. Checked against the oracle on
+ragged shapes (N not a multiple of 512 or of 64, K not a multiple of 64, fewer
+k-slices than ring stages, K = 0), on every epilog family it serves, with many
+tiles per CTA pair, under both schedules, and through a bounded wait that runs
+out."""
 import numpy as np
 import pytest
 
@@ -20,7 +22,9 @@ if not torch.cuda.is_available():
 import gemm_epilogue_tmem_gb300 as gf  # noqa: E402
 
 WIDE = 3
-SHAPES = [(3000, 2568, 264), (1000, 2560, 64), (700, 1088, 520), (520, 1032, 0)]
+SHAPES = [(3000, 2568, 264), (1000, 2560, 64), (700, 1088, 520), (520, 1032, 0),
+          # longer k loops: head, middle and tail of the half schedule all present
+          (1000, 1088, 1344), (600, 2568, 2056)]
 
 
 def _wide(plan):
@@ -76,7 +80,7 @@ def test_wide_drelu_bgrad(M, N, K, mode):
     assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
 
 
-@pytest.mark.parametrize("M,N,K", SHAPES[:3])
+@pytest.mark.parametrize("M,N,K", SHAPES[:3] + SHAPES[4:])
 def test_wide_none_and_bias(M, N, K):
     d = synth.BF16
     A = synth.normal((M, K), d, 43, synth.TID_A, 1.0)
@@ -90,7 +94,7 @@ def test_wide_none_and_bias(M, N, K):
     assert_close(to_host_f32(out), oracle.decode(oracle.epilog_none(A, B, d), d), what="NONE")
 
 
-@pytest.mark.parametrize("M,N,K", SHAPES[:3])
+@pytest.mark.parametrize("M,N,K", SHAPES[:3] + SHAPES[4:])
 def test_wide_gelu_forward_backward(M, N, K):
     d = synth.BF16
     X = synth.normal((M, K), d, 44, synth.TID_A, 1.0)
@@ -217,3 +221,38 @@ def test_wide_wait_limit():
     ref = torch.relu(X.float() @ W.float())
     assert float((out.float() - ref).abs().max() / ref.abs().max()) < 2e-2
     plan.free()
+
+
+def test_wide_many_tiles_long_k():
+    """Several wide tiles per CTA pair with 21 k-slices each: the head and
+    tail half-passes of consecutive tiles interleave with their drains."""
+    M, N, K = 4096, 8192, 1344
+    X = synth.normal((M, K), synth.F16, 48, synth.TID_A, 1.0)
+    W = synth.normal((K, N), synth.F16, 48, synth.TID_B, 1 / np.sqrt(K))
+    b = synth.normal((N,), synth.F16, 48, synth.TID_BIAS, 0.1)
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    aux = torch.empty((M // 32, N), dtype=torch.int32, device="cuda")
+    fwd = gf.gf_matmul_plan(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    d = _wide(fwd)
+    assert (M // 256) * (N // 512) >= 3 * (d["grid"] // 2)
+    gf.gf_matmul_execute(fwd, to_dev(X, 0), to_dev(W, 0), bias=to_dev(b, 0), out=out, aux_out=aux)
+    assert gf.gf_plan_status(fwd) == gf.GF_OK
+    fwd.free()
+    y_o, z_o = oracle.relu_bias(X, W, b, oracle.F16)
+    assert_close(to_host_f32(out), oracle.decode(y_o, 0), what="Y")
+    outside, _ = mask_mismatch(unpack_words(to_host_words(aux), M), z_o)
+    assert outside == 0
+
+    Wt = synth.normal((N, K), synth.F16, 48, synth.TID_W2, 1 / np.sqrt(K))
+    words = synth.mask_words(M, N, 48)
+    bgrad = torch.empty((N,), dtype=torch.float32, device="cuda")
+    bwd = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                               gf.GF_B_NK)
+    _wide(bwd)
+    gf.gf_matmul_execute(bwd, to_dev(X, 0), to_dev(Wt, 0), out=out, aux_in=to_dev(words, 0),
+                         bgrad=bgrad)
+    assert gf.gf_plan_status(bwd) == gf.GF_OK
+    bwd.free()
+    dz_o, bgrad_o, _ = oracle.drelu_bgrad(X, Wt, words, oracle.F16, oracle.B_NK)
+    assert_close(to_host_f32(out), oracle.decode(dz_o, 0), what="dZ")
+    assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
