@@ -236,7 +236,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     nthreads = os.cpu_count() or 1
-    per_step_rows = max(1, args.ref_step_rows)
+    # bounded work per step: about 200 sampled rows per GEMM over the whole run
+    per_step_rows = max(1, min(args.ref_step_rows, 200 // max(args.steps, 1)))
     for _ in range(args.warmup):
         oracle_sample(1, 1, nthreads)
     times, flops_tot = [], 0.0
@@ -531,7 +532,13 @@ def run_gpu(args):
         ref_rows = {}
         fl, sec, desc = oracle_sample(args.ref_rows, args.ref_rows, nthreads, outputs=ref_rows)
         cpu = {"value": fl / sec / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-               "sample": desc, "seconds": sec}
+               "sample": desc, "seconds": sec,
+               # the whole step at this rate (an extrapolation from the sampled rows)
+               "extrapolated_full_step_s": 2 * FLOP_PER_GEMM / (fl / sec)}
+        fl1, sec1, _ = oracle_sample(4, 4, 1, offset=1)
+        cpu["single_thread"] = {"value": fl1 / sec1 / 1e12, "unit": "TFLOP/s",
+                                "sample": "4 sampled rows of each GEMM, 1 thread",
+                                "seconds": sec1}
         n_f, n_b = len(ref_rows["rows_fwd"]), len(ref_rows["rows_bwd"])
         parity = sampled_parity({"Y": dev_rows["Y"][:n_f], "aux_rows": dev_rows["aux_rows"][:n_f],
                                  "dZ": dev_rows["dZ"][:n_b]}, ref_rows)
@@ -952,7 +959,7 @@ def run_compare_schedules(args):
 
     for rnd in range(2):
         for name, (plan, fn) in cfgs.items():
-            print(json.dumps({"config": name, "round": rnd, "shape": [M, N, K], **run(fn)}),
+            print(json.dumps({"config": name, "repeat": rnd, "shape": [M, N, K], **run(fn)}),
                   flush=True)
     for plan, _ in cfgs.values():
         if plan is not None:
@@ -972,7 +979,7 @@ def main():
     ap.add_argument("--kernel", type=int, default=0,
                     help="0 plan's choice, 1 single CTA, 2 pair, 3 pair with 256 x 512 tiles")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gf", choices=["gf", "reference"])
     ap.add_argument("--ref-rows", type=int, default=64,
