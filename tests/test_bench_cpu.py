@@ -1,0 +1,53 @@
+"""Host-side pieces of bench.py that need no GPU: the sampled-row parity
+summary (error norms and the ReLU-mask band rule) and the recorded DRAM
+traffic lookup."""
+import numpy as np
+
+import bench
+
+
+def _ref(rows, z):
+    y = np.maximum(z, 0).astype(np.float32)
+    return {"rows_fwd": rows, "rows_bwd": rows, "Y": y, "z": z, "dZ": y.copy()}
+
+
+def _words_for(rows, bits):
+    """aux word rows (r // 32) of each sampled row, holding that row's bits"""
+    w = np.zeros((len(rows), bits.shape[1]), dtype=np.uint32)
+    for i, r in enumerate(rows):
+        w[i] = bits[i].astype(np.uint32) << np.uint32(r % 32)
+    return w
+
+
+def test_sampled_parity_exact_and_band():
+    rng = np.random.default_rng(0)
+    rows = np.array([3, 40, 77], dtype=np.int64)
+    z = rng.standard_normal((3, 64)).astype(np.float32)
+    z[0, 5] = 1e-6  # inside the band |z| < 1e-3 max|z| of its row
+    ref = _ref(rows, z)
+    bits = (z > 0).astype(np.uint8)
+    bits[0, 5] ^= 1  # a flip inside the band is allowed
+    dev = {"Y": ref["Y"].copy(), "dZ": ref["dZ"].copy(), "aux_rows": _words_for(rows, bits)}
+    r = bench.sampled_parity(dev, ref)
+    assert r["pass"] and r["Y"]["nmax"] == 0.0 and r["dZ"]["rel_l2"] == 0.0
+    assert r["mask_mismatch_in_band"] == 1 and r["mask_mismatch_outside_band"] == 0
+
+
+def test_sampled_parity_catches_errors():
+    rng = np.random.default_rng(1)
+    rows = np.array([0, 33], dtype=np.int64)
+    z = rng.standard_normal((2, 32)).astype(np.float32) + 3.0  # all well outside the band
+    ref = _ref(rows, z)
+    bits = (z > 0).astype(np.uint8)
+    bits[1, 7] ^= 1
+    dev = {"Y": ref["Y"] * 1.05, "dZ": ref["dZ"].copy(), "aux_rows": _words_for(rows, bits)}
+    r = bench.sampled_parity(dev, ref)
+    assert not r["pass"]
+    assert r["mask_mismatch_outside_band"] == 1
+    assert abs(r["Y"]["rel_l2"] - 0.05) < 1e-6
+
+
+def test_recorded_traffic_matches_sources():
+    # the committed profile is read back only while its digest matches the sources
+    t = bench.recorded_traffic()
+    assert t is None or (len(t) == 2 and all(v > 3e9 for v in t))
