@@ -586,6 +586,8 @@ def run_profile_case(args):
     import gemm_epilogue_tmem_gb300 as gf
 
     m, n, k = (int(x) for x in args.profile_case.split(","))
+    if args.epilog in ("swiglu_save", "dswiglu"):
+        return run_profile_case_swiglu(args, m, n, k)
     epi = {"relu_aux_bias": gf.GF_EPILOG_RELU_AUX_BIAS, "drelu_bgrad": gf.GF_EPILOG_DRELU_BGRAD,
            "none": gf.GF_EPILOG_NONE, "relu_bias": gf.GF_EPILOG_RELU_BIAS}[args.epilog]
     layout = gf.GF_B_NK if epi == gf.GF_EPILOG_DRELU_BGRAD else gf.GF_B_KN
@@ -611,6 +613,47 @@ def run_profile_case(args):
             gf.gf_matmul_execute(plan, A, B, out=out, aux_in=aux, bgrad=bgrad, stream=sp)
         else:
             gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=aux, stream=sp)
+    torch.cuda.synchronize()
+    st = gf.gf_plan_status(plan, sp)
+    print(json.dumps({"profile_case": [m, n, k], "epilog": args.epilog, "status": st,
+                      "plan": gf.gf_plan_describe(plan)}))
+    plan.free()
+    return 0 if st == gf.GF_OK else 1
+
+
+def run_profile_case_swiglu(args, m, n, k):
+    """--profile-case M,I,H with --epilog swiglu_save (gate+up forward saving
+    g and u) or dswiglu (dh = dout Wd with the dSwiGLU epilogue), bf16."""
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+    gf.build()
+    synth.build_cuda()
+    sp = torch.cuda.current_stream().cuda_stream
+    bf = torch.bfloat16
+    dev = torch.device("cuda", 0)
+
+    def filled(shape, tid, sigma):
+        t = torch.empty(shape, dtype=bf, device=dev)
+        synth.dev_normal(t, synth.BF16, 0, tid, sigma, sp)
+        return t
+
+    outs = [torch.empty((m, n), dtype=bf, device=dev) for _ in range(3)]
+    if args.epilog == "swiglu_save":
+        x, wg, wu = filled((m, k), synth.TID_A, 1.0), filled((n, k), synth.TID_WG, 0.02), \
+            filled((n, k), synth.TID_WU, 0.02)
+        plan = gf.gf_swiglu_plan(m, n, k, gf.GF_BF16, save_gu=True)
+        fn = lambda: gf.gf_swiglu_execute(plan, x, wg, wu, *outs, stream=sp)  # noqa: E731
+    else:
+        dout, wd = filled((m, k), synth.TID_DOUT, 1.0), filled((k, n), synth.TID_WD, 0.02)
+        g, u = filled((m, n), synth.TID_G_SAVED, 1.0), filled((m, n), synth.TID_U_SAVED, 1.0)
+        plan = gf.gf_dswiglu_plan(m, n, k, gf.GF_BF16)
+        fn = lambda: gf.gf_dswiglu_execute(plan, dout, wd, g, u, outs[0], outs[1],  # noqa: E731
+                                           stream=sp)
+    if args.kernel:
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, args.kernel)
+    for _ in range(args.warmup + args.steps):
+        fn()
     torch.cuda.synchronize()
     st = gf.gf_plan_status(plan, sp)
     print(json.dumps({"profile_case": [m, n, k], "epilog": args.epilog, "status": st,
@@ -975,7 +1018,8 @@ def main():
     ap.add_argument("--profile-case", default="",
                     help="M,N,K: run one fused GEMM of this shape (for ncu captures)")
     ap.add_argument("--epilog", default="relu_aux_bias",
-                    choices=["relu_aux_bias", "drelu_bgrad", "none", "relu_bias"])
+                    choices=["relu_aux_bias", "drelu_bgrad", "none", "relu_bias", "swiglu_save",
+                             "dswiglu"])
     ap.add_argument("--kernel", type=int, default=0,
                     help="0 plan's choice, 1 single CTA, 2 pair, 3 pair with 256 x 512 tiles")
     ap.add_argument("--gpus", type=int, default=1)
