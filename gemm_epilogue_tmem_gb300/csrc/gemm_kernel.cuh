@@ -291,9 +291,27 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   const int nch = min(BN / 32, (p.N - n0 + 31) / 32);  // chunks with columns below N
   if (nch <= 0) return;
 
+  // the saved 16-bit activations are read coalesced when the staging buffer
+  // is there: lane l loads 16 bytes of row 8g + l/4 (4 lanes per 64-byte row
+  // segment), and transpose_side() hands each lane its own row afterwards
+  constexpr bool kCoalesced = STG && (EPI == EPI_DSWIGLU || EPI == EPI_DGELU_BGRAD);
   auto load_side = [&](int col0, uint4 (&sd)[kSideN]) {
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_DGELU_BGRAD) {
+    if constexpr (kCoalesced) {
+      const uint32_t pc = lane & 3u;
+      const int col = col0 + 8 * (int)pc;
+#pragma unroll
+      for (int in = 0; in < (EPI == EPI_DSWIGLU ? 2 : 1); ++in) {
+        const T* base = reinterpret_cast<const T*>(in == 0 ? p.aux_in : p.aux_in2);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int r = row0w + 8 * g + (int)(lane >> 2);
+          sd[4 * in + g] = r < p.M && col < p.N
+                               ? __ldg(reinterpret_cast<const uint4*>(base + (size_t)r * p.N + col))
+                               : zero;
+        }
+      }
+    } else if constexpr (EPI == EPI_DSWIGLU || EPI == EPI_DGELU_BGRAD) {
       const T* ap = reinterpret_cast<const T*>(p.aux_in) + (size_t)row * p.N + col0;
 #pragma unroll
       for (int g = 0; g < 4; ++g)
@@ -362,8 +380,28 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     }
     uint4 cur[kSideN];
+    if constexpr (kCoalesced) {
+      // through the staging buffer: rows as loaded -> this lane's row
 #pragma unroll
-    for (int i = 0; i < kSideN; ++i) cur[i] = sd[i];
+      for (int in = 0; in < (EPI == EPI_DSWIGLU ? 2 : 1); ++in) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t r = 8u * g + (lane >> 2);
+          const uint32_t pc = lane & 3u;
+          const uint4 v4 = sd[4 * in + g];
+          st_shared_v4(stg + r * 64u + ((pc ^ ((r >> 1) & 3u)) << 4), v4.x, v4.y, v4.z, v4.w);
+        }
+        __syncwarp();
+        const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+        for (uint32_t pc = 0; pc < 4; ++pc)
+          cur[4 * in + pc] = ld_shared_v4(stg + lane * 64u + ((pc ^ sw) << 4));
+        __syncwarp();
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < kSideN; ++i) cur[i] = sd[i];
+    }
     if (c + 1 < nch) {  // next chunk's loads, in flight while this one is processed
       if (has_acc) {
         tmem_ld_32x32b_x32(t_row + 32u * (c + 1), ra);

@@ -46,11 +46,14 @@ namespace gf {
 // slower with eight warps than with four.)
 GF_HD constexpr bool pair_epi8(int epi, bool wide) { return wide && epi >= 0; }
 
-// Output staging through shared memory (64-byte row segments): the wide
+// A 2 KB shared-memory staging buffer per epilogue warp: 64-byte row-segment
+// output stores, and coalesced loads of saved 16-bit activations. The wide
 // tiles, and on 256 x 256 tiles the epilogs that store two or three 16-bit
-// outputs per element (one ring stage makes room for it).
+// outputs per element or read saved activations (one ring stage makes room
+// for it where the bias-gradient scratch has not already).
 GF_HD constexpr bool pair_stg(int epi, bool wide) {
-  return wide || epi == EPI_GELU_AUX_BIAS || epi == EPI_SWIGLU_SAVE || epi == EPI_DSWIGLU;
+  return wide || epi == EPI_GELU_AUX_BIAS || epi == EPI_SWIGLU_SAVE || epi == EPI_DSWIGLU ||
+         epi == EPI_DGELU_BGRAD;
 }
 
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
