@@ -256,3 +256,20 @@ def test_wide_many_tiles_long_k():
     dz_o, bgrad_o, _ = oracle.drelu_bgrad(X, Wt, words, oracle.F16, oracle.B_NK)
     assert_close(to_host_f32(out), oracle.decode(dz_o, 0), what="dZ")
     assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
+
+
+def test_wide_row_bias():
+    """A per-row bias (bias[m]) through the wide tiles, whose column-bias
+    prefetch into shared memory must then stay unused."""
+    M, N, K = 1000, 1088, 1344
+    X = synth.normal((M, K), synth.F16, 49, synth.TID_A, 1.0)
+    W = synth.normal((K, N), synth.F16, 49, synth.TID_B, 1 / np.sqrt(K))
+    b = synth.normal((M,), synth.F16, 49, synth.TID_BIAS, 0.5)
+    out = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    plan = gf.gf_matmul_plan(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_ROW)
+    _wide(plan)
+    gf.gf_matmul_execute(plan, to_dev(X, 0), to_dev(W, 0), bias=to_dev(b, 0), out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    y_o, _ = oracle.relu_bias(X, W, b, oracle.F16, oracle.B_KN, oracle.BIAS_ROW)
+    assert_close(to_host_f32(out), oracle.decode(y_o, 0), what="Y (row bias)")
