@@ -32,7 +32,10 @@
 //     the 256-wide tile. The price is a single accumulator: the epilogue
 //     drains half 0 and releases it, then half 1; the MMA thread starts the
 //     next tile on half 0 over the stages already loaded and adds the half-1
-//     products of those stages once half 1 is free.
+//     products of those stages once half 1 is free, and runs a tile's last
+//     ring of k-slices into half 0 first so that half 0's drain starts early.
+//     Eight epilogue warps (two per TMEM lane quarter, each with half of the
+//     columns) keep that exposed drain short.
 //   - Teardown: drains, then a cluster barrier, then a pair TMEM dealloc.
 #pragma once
 
