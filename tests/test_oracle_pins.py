@@ -86,6 +86,18 @@ def test_hand_drelu_bgrad():
     assert np.array_equal(bgrad, np.array(g["drelu_bgrad"], dtype=np.float32))
 
 
+def test_hand_drelu_row_ids():
+    # rows 3 and 1 alone, with their global row indices, take the mask bits
+    # of rows 3 and 1 (word bits 3 and 1), not of rows 0 and 1
+    g = gold()
+    A, B = f16(g["A"]), f16(g["B_kn"])
+    words = np.array(g["drelu_words"], dtype=np.uint32)
+    out, bgrad, _ = oracle.drelu_bgrad(A[[3, 1]], np.ascontiguousarray(B.T), words, oracle.F16,
+                                       oracle.B_NK, row_ids=np.array([3, 1]))
+    assert bgrad is None
+    assert np.array_equal(vals(out), np.array(g["drelu_dz"], dtype=np.float32)[[3, 1]])
+
+
 # -------------------------------------------------------------- number formats
 def _special_f32():
     r = np.random.default_rng(0)
