@@ -910,18 +910,42 @@ def run_small_workloads(args, gf, torch, dev, sp, peak, pk):
     Nr = rc.tensors["B"].shape[1]
     Yr = torch.empty((Mr, Nr), dtype=f16, device=dev)
     plan = gf.gf_matmul_plan(Mr, Nr, Kr, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_ROW)
+    # 20 launches captured once (launch overhead of the host removed), the
+    # same with the k split switched off, and cuBLAS + torch unfused
+    nosplit = gf.gf_matmul_plan(Mr, Nr, Kr, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_ROW)
+    gf.gf_plan_set_option(nosplit, gf.GF_OPT_SPLIT_K, 1)
+    graphs = {}
+    for name, pl in (("fused_graph", plan), ("fused_graph_no_split", nosplit)):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                cs = torch.cuda.current_stream().cuda_stream
+                for _ in range(20):
+                    gf.gf_matmul_execute(pl, A, B, bias=bias, out=Yr, stream=cs)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        graphs[name] = g
     ms = _interleaved(torch, {
         "fused": lambda: gf.gf_matmul_execute(plan, A, B, bias=bias, out=Yr, stream=sp),
+        "fused_graph": graphs["fused_graph"].replay,
+        "fused_graph_no_split": graphs["fused_graph_no_split"].replay,
         "torch_unfused": lambda: torch.relu(torch.addmm(bias[:, None], A, B)),
     }, reps=200)
+    g_ms = ms["fused_graph"] / 20
     flop = 2.0 * Mr * Nr * Kr
     out.append({"workload": f"relu_bias_rowbias_fp16_{Mr}x{Nr}x{Kr}",
                 "value": flop / (ms["fused"] * 1e-3) / 1e12, "ms_per_step": ms["fused"],
-                "us_per_step": 1e3 * ms["fused"], "torch_unfused_us": 1e3 * ms["torch_unfused"],
+                "us_per_step": 1e3 * ms["fused"], "graph_replay_us": 1e3 * g_ms,
+                "graph_replay_tflops": flop / (g_ms * 1e-3) / 1e12,
+                "graph_replay_no_split_us": 1e3 * ms["fused_graph_no_split"] / 20,
+                "torch_unfused_us": 1e3 * ms["torch_unfused"],
                 "fused_vs_torch_unfused": ms["torch_unfused"] / ms["fused"], "launches_per_step": 1,
                 "plan": gf.gf_plan_describe(plan), "l2": "inputs fit in L2 (latency-bound)",
-                "status_ok": gf.gf_plan_status(plan, sp) == gf.GF_OK})
+                "status_ok": gf.gf_plan_status(plan, sp) == gf.GF_OK and
+                gf.gf_plan_status(nosplit, sp) == gf.GF_OK})
+    del graphs
     plan.free()
+    nosplit.free()
     return out
 
 

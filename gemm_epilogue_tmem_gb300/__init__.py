@@ -22,7 +22,7 @@ __all__ = [
     "GF_EPILOG_BIAS", "GF_EPILOG_GELU_BIAS", "GF_EPILOG_GELU_AUX_BIAS", "GF_EPILOG_DGELU_BGRAD",
     "GF_BIAS_COL", "GF_BIAS_ROW", "GF_B_KN", "GF_B_NK", "GF_BGRAD_TWO_PASS", "GF_BGRAD_ATOMIC",
     "GF_OPT_BGRAD_MODE", "GF_OPT_WAIT_LIMIT_US", "GF_OPT_TILE_N", "GF_OPT_FAULT_DROP_LOAD",
-    "GF_OPT_KERNEL", "GF_OPT_GROUP_M", "GF_OPT_L2_HINTS", "GF_OPT_SCHEDULE",
+    "GF_OPT_KERNEL", "GF_OPT_GROUP_M", "GF_OPT_L2_HINTS", "GF_OPT_SCHEDULE", "GF_OPT_SPLIT_K",
     "GfError", "Plan", "build", "lib", "gf_matmul_plan", "gf_matmul_plan_ex",
     "gf_matmul_execute", "gf_plan_status", "gf_plan_set_option", "gf_plan_describe",
     "gf_plan_free", "gf_status_string", "gf_last_error", "gf_drelu_bgrad_noalloc",
@@ -46,6 +46,7 @@ GF_BGRAD_TWO_PASS, GF_BGRAD_ATOMIC = 0, 1
 # gf_option
 GF_OPT_BGRAD_MODE, GF_OPT_WAIT_LIMIT_US, GF_OPT_TILE_N, GF_OPT_FAULT_DROP_LOAD = 0, 1, 2, 3
 GF_OPT_KERNEL, GF_OPT_GROUP_M, GF_OPT_L2_HINTS, GF_OPT_SCHEDULE = 4, 5, 6, 7
+GF_OPT_SPLIT_K = 8
 # fp32 partial sums the allocation-free DRELU_BGRAD entry point can hold
 GF_NOALLOC_MAX_PARTIALS = 2097152
 
@@ -83,6 +84,8 @@ def lib(path: str | None = None):
         L.gf_plan_set_option.argtypes = [_P, _I32, _I64]
         L.gf_plan_describe.restype = _I32
         L.gf_plan_describe.argtypes = [_P, _P, _P, _P, _P, _P]
+        L.gf_plan_k_splits.restype = _I32
+        L.gf_plan_k_splits.argtypes = [_P, _P]
         L.gf_plan_free.restype = None
         L.gf_plan_free.argtypes = [_P]
         L.gf_status_string.restype = ctypes.c_char_p
@@ -235,8 +238,12 @@ def gf_plan_describe(plan: Plan) -> dict:
     rc = lib().gf_plan_describe(plan.handle, *(ctypes.byref(v) for v in vals), ctypes.byref(ws))
     if rc != GF_OK:
         raise GfError(rc, "gf_plan_describe")
+    ks = ctypes.c_int32()
+    rc = lib().gf_plan_k_splits(plan.handle, ctypes.byref(ks))
+    if rc != GF_OK:
+        raise GfError(rc, "gf_plan_k_splits")
     return {"tile_m": vals[0].value, "tile_n": vals[1].value, "stages": vals[2].value,
-            "grid": vals[3].value, "workspace_bytes": ws.value}
+            "grid": vals[3].value, "workspace_bytes": ws.value, "k_splits": ks.value}
 
 
 def gf_plan_free(plan: Plan) -> None:

@@ -532,6 +532,102 @@ __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float*
   named_bar_sync(1, NT);
 }
 
+// Split k: the k-blocks of tile t are shared by `ks` CTAs. Each leaves its
+// fp32 partial sum (its accumulator, one row per epilogue thread) in the
+// workspace and counts itself in the tile's counter; the CTA that counts last
+// adds the partials in split order -- the sum does not depend on which split
+// finishes last -- writes it back into its accumulator and runs the epilogue.
+// No CTA waits for another. Returns true in that last CTA. Called by the 128
+// epilogue threads (ep_tid 0..127, thread = accumulator row 32 q + lane).
+// A partial is stored as [BN / 4][128 rows] float4 pieces, so that the 32
+// lanes of a warp (32 consecutive rows) move 512 contiguous bytes per access.
+template <int BN>
+__device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_row, int t, int s,
+                                              int ks, int q, uint32_t lane, int ep_tid,
+                                              volatile int* last_flag) {
+  constexpr int kPart = kBM * BN / 4;  // float4 pieces of one partial
+  const int row = 32 * q + static_cast<int>(lane);
+  float4* tile_ws = reinterpret_cast<float4*>(p.splitk_ws) + static_cast<size_t>(t) * ks * kPart;
+  float4* mine = tile_ws + static_cast<size_t>(s) * kPart + row;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), v);
+    tmem_ld_wait_tied(v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      __stcg(mine + (c / 4 + j) * kBM,
+             make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+  }
+  __threadfence();
+  named_bar_sync(1, 128);
+  if (ep_tid == 0) {
+    const int done = atomicAdd(p.splitk_cnt + t, 1);
+    const int last = done == ks - 1 ? 1 : 0;
+    if (last) p.splitk_cnt[t] = 0;  // every split has counted: ready for the next launch
+    *last_flag = last;
+  }
+  named_bar_sync(1, 128);
+  if (*last_flag == 0) return false;
+  __threadfence();
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    // this CTA's own partial is still in its accumulator
+    uint32_t own[32];
+    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), own);
+    tmem_ld_wait_tied(own);
+    const float4* src = tile_ws + (c / 4) * kBM + row;
+    float acc[32];
+#pragma unroll 1
+    for (int sp = 0; sp < ks; sp += 2) {
+      // two splits' pieces in flight at once; a split's own piece from TMEM
+      float4 x[8], y[8];
+      const float4* a = src + static_cast<size_t>(sp) * kPart;
+      const float4* b = a + kPart;
+      const bool has_b = sp + 1 < ks;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        x[j] = sp == s ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                     __uint_as_float(own[4 * j + 2]),
+                                     __uint_as_float(own[4 * j + 3]))
+                       : __ldcg(a + j * kBM);
+        y[j] = !has_b ? make_float4(0.f, 0.f, 0.f, 0.f)
+               : sp + 1 == s
+                   ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                 __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]))
+                   : __ldcg(b + j * kBM);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (sp == 0) {
+          acc[4 * j] = x[j].x;
+          acc[4 * j + 1] = x[j].y;
+          acc[4 * j + 2] = x[j].z;
+          acc[4 * j + 3] = x[j].w;
+        } else {
+          acc[4 * j] += x[j].x;
+          acc[4 * j + 1] += x[j].y;
+          acc[4 * j + 2] += x[j].z;
+          acc[4 * j + 3] += x[j].w;
+        }
+        if (has_b) {
+          acc[4 * j] += y[j].x;
+          acc[4 * j + 1] += y[j].y;
+          acc[4 * j + 2] += y[j].z;
+          acc[4 * j + 3] += y[j].w;
+        }
+      }
+    }
+    uint32_t u[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(acc[j]);
+    tmem_st_32x32b_x32(t_row + static_cast<uint32_t>(c), u);
+  }
+  tmem_st_wait();
+  return true;
+}
+
 template <int EPI, typename T, bool B_MN, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_epilog_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -559,8 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 44);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);  // [4][BN]
 
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 48);
+
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
+  // work units: tile t, k-split s as unit t * ks + s (ks = 1: the tiles)
+  const int ks = p.k_splits > 1 ? p.k_splits : 1;
+  const int kps = ks > 1 ? p.kb_per_split : p.num_k_blocks;
+  const int units = p.num_tiles * ks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -601,7 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint64_t pol_a = l2_policy(p.l2_hint_a);
       const uint64_t pol_b = l2_policy(p.l2_hint_b);
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const int t = u / ks;
+        const int kb0 = (u - t * ks) * kps;
+        const int kb1 = min(p.num_k_blocks, kb0 + kps);
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
@@ -609,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a 3-D box always moves all BN / 64 chunks (zero fill past N)
         const uint32_t bytes =
             C::kABytes + (B_MN && !p.b_mn_3d ? nbox * 64 * kBK * 2 : C::kStageBBytes);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
             ok = false;
@@ -656,7 +761,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++it) {
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+        const int kb0 = (u % ks) * kps;
+        const int kb1 = min(p.num_k_blocks, kb0 + kps);
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded(tempty0 + 8u * buf, use ^ 1u, abort_flag, p.wait_limit_ns)) {
@@ -669,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(tfull0 + 8u * buf);  // acc is all zeros: nothing to multiply
           continue;
         }
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
             ok = false;
@@ -687,10 +794,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // 64-column chunks 64*128 bytes apart (LBO), 8-k groups 1024 (SBO).
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+            umma_f16(d_tmem, adesc, bdesc, idesc, accum);
             if constexpr (NB == 2) {  // second accumulator: columns [BN, 2 BN) of the set
               const uint64_t bdesc2 = sdesc_sw128(b_base + C::kBBytes + kk * 32, 16, 1024);
-              umma_f16(d_tmem + BN, adesc, bdesc2, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_f16(d_tmem + BN, adesc, bdesc2, idesc, accum);
             }
           }
           umma_commit(empty0 + 8u * stage);  // frees the stage once these MMAs finish
@@ -712,11 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // the TMEM lane quarter this warp may access
     const int ep_tid = threadIdx.x - 64;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
+      const int t = u / ks;
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1) & 1u;
       bool ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
-      if constexpr (epi_has_bgrad(EPI)) {
+      if (epi_has_bgrad(EPI) || ks > 1) {
         // the four warps meet at named barriers below: they must agree
         ok = !named_bar_red_or(1, 128, !ok);
       }
@@ -731,6 +840,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
 
+      if (ks > 1 && !splitk_reduce<BN>(p, t_row, t, u - t * ks, ks, q, lane, ep_tid, last_flag)) {
+        // a partial sum, handed over through the workspace: buffer free again
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8u * buf);
+        continue;
+      }
       epilogue_drain<EPI, T, BN>(p, t_row, m0, n0, q, lane, red);
       // accumulator buffer drained: the MMA warp may reuse it
       tc_fence_before();

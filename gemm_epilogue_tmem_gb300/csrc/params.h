@@ -77,6 +77,12 @@ struct GemmParams {
   int* tile_counter;  // CTA-pair kernel: global tile counter of the dynamic schedule (null: static)
   int32_t b_mn_3d;    // MN-major B through a 3-D map: one box per k-slice brings every
                       // 64-column chunk of the tile (0: one 2-D box per chunk)
+  // single-CTA kernel, split k: each tile's k-blocks are shared by k_splits
+  // CTAs, kb_per_split each (the last may have fewer); 0 or 1: no split
+  int32_t k_splits;
+  int32_t kb_per_split;
+  float* splitk_ws;     // fp32 partial sums [num_tiles][k_splits][tile_n / 4][128] float4
+  int32_t* splitk_cnt;  // [num_tiles] splits done per tile; zero between launches
 };
 
 }  // namespace gf

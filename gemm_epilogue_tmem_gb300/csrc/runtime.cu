@@ -49,6 +49,12 @@ struct gf_plan {
   int32_t* d_status;     // device status word (bounded-wait time-outs)
   float* d_partials;     // [num_m_blocks][n] fp32, DRELU_BGRAD two-pass only
   size_t partial_bytes;
+  int forced_split;      // 0 the plan's choice, 1 no split, else k-splits per tile
+  int k_splits;          // single-CTA kernel: CTAs sharing the k-blocks of one tile
+  int kb_per_split;
+  void* d_splitk;        // split-k partial sums, then the per-tile counters
+  size_t splitk_bytes;   // capacity of d_splitk
+  size_t splitk_cnt_offset;
 };
 
 namespace {
@@ -62,6 +68,8 @@ gf_status fail(gf_status s) {
 
 constexpr int kBM = 128;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+// largest split-k partial-sum workspace a plan takes
+constexpr size_t kMaxSplitkBytes = size_t(256) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuCtxGetDevice_v2000 g_ctx_get_device = nullptr;
@@ -153,6 +161,8 @@ void plan_tiles(gf_plan* p) {
   p->num_m_blocks = static_cast<int>(mblocks);
   p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
   p->group_m = p->forced_group_m > 0 ? p->forced_group_m : 8;
+  p->k_splits = 1;
+  p->kb_per_split = p->num_k_blocks;
   // The CTA-pair kernel (256 x 256 tiles over two SMs; 256 x 128 per operand
   // with two B operands) moves 2/3 of the operand bytes per flop of the
   // single-CTA tile; take it when its tiles fill the resident pairs, else the
@@ -203,7 +213,73 @@ void plan_tiles(gf_plan* p) {
   p->num_n_blocks = static_cast<int>((p->n + tn - 1) / tn);
   const int64_t tiles = mblocks * p->num_n_blocks;
   p->num_tiles = static_cast<int>(tiles);
-  p->grid = static_cast<int>(p->one_tile_per_cta || tiles < p->num_sms ? tiles : p->num_sms);
+  // Split k: when the tiles leave most SMs idle, the k-blocks of each tile
+  // are shared by several CTAs whose fp32 partial sums meet in the plan's
+  // workspace; the last CTA of a tile to finish adds them and runs the
+  // epilogue. The plan's choice: when k has at least 16 blocks and the tiles
+  // fill at most half the SMs, as many splits as the idle SMs take, at most
+  // 8 and at most sqrt(k-blocks / 2) (a split's mainloop then stays longer
+  // than the partial-sum hand-over, which moves (splits + 1) x 64 KB).
+  int want = 0;
+  if (!dual && p->num_k_blocks >= 2 && tiles > 0) {
+    if (p->forced_split >= 2) {
+      want = p->forced_split;
+    } else if (p->forced_split == 0 && p->num_k_blocks >= 16 && 2 * tiles <= p->num_sms) {
+      int r = 1;
+      while ((r + 1) * (r + 1) <= p->num_k_blocks / 2) ++r;
+      const int64_t idle = p->num_sms / tiles;
+      want = static_cast<int>(idle < r ? idle : r);
+      if (want > 8) want = 8;
+    }
+  }
+  if (want >= 2) {
+    const int kps = (p->num_k_blocks + want - 1) / want;
+    const int ks = (p->num_k_blocks + kps - 1) / kps;  // every split gets k-blocks
+    const size_t ws = static_cast<size_t>(tiles) * ks * kBM * tn * 4;
+    if (ks >= 2 && ws <= kMaxSplitkBytes) {
+      p->k_splits = ks;
+      p->kb_per_split = kps;
+    }
+  }
+  const int64_t units = tiles * p->k_splits;
+  p->grid = static_cast<int>(p->one_tile_per_cta || units < p->num_sms ? units : p->num_sms);
+}
+
+// The split-k workspace of the plan's current tiling: fp32 partial sums
+// [tiles][splits][tile_n / 4][128] float4, then one zeroed counter per tile. Grown when
+// too small; on failure the plan falls back to no split.
+gf_status ensure_splitk(gf_plan* p) {
+  if (p->k_splits < 2) return GF_OK;
+  const size_t ws = static_cast<size_t>(p->num_tiles) * p->k_splits * kBM * p->tile_n * 4;
+  const size_t need = ws + static_cast<size_t>(p->num_tiles) * 4;
+  gf_status st = GF_OK;
+  if (need > p->splitk_bytes) {
+    if (p->d_splitk) cudaFree(p->d_splitk);
+    p->d_splitk = nullptr;
+    p->splitk_bytes = 0;
+    if (cudaMalloc(&p->d_splitk, need) == cudaSuccess)
+      p->splitk_bytes = need;
+    else
+      st = GF_ERR_OUT_OF_MEMORY;
+  }
+  if (st == GF_OK) {
+    p->splitk_cnt_offset = ws;
+    if (cudaMemset(static_cast<char*>(p->d_splitk) + ws, 0, static_cast<size_t>(p->num_tiles) * 4) !=
+        cudaSuccess)
+      st = GF_ERR_CUDA;
+  }
+  if (st != GF_OK) {
+    cudaGetLastError();
+    p->forced_split = 1;
+    plan_tiles(p);
+  }
+  return st;
+}
+
+// plan_tiles, then the workspace the new tiling needs
+gf_status replan(gf_plan* p) {
+  plan_tiles(p);
+  return ensure_splitk(p);
 }
 
 // Validation, device checks, tile choice and workspace: the plan step of
@@ -324,6 +400,13 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
       return nullptr;
     }
   }
+  if (ensure_splitk(p) != GF_OK) {
+    if (p->d_partials) cudaFree(p->d_partials);
+    cudaFree(p->d_status);
+    free(p);
+    fail(GF_ERR_OUT_OF_MEMORY);
+    return nullptr;
+  }
   return p;
 }
 
@@ -420,6 +503,13 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.l2_hint_a = p->l2_hint_a;
   prm.l2_hint_b = p->l2_hint_b;
   prm.b_mn_3d = b_mn_3d ? 1 : 0;
+  if (p->k_splits > 1) {
+    prm.k_splits = p->k_splits;
+    prm.kb_per_split = p->kb_per_split;
+    prm.splitk_ws = static_cast<float*>(p->d_splitk);
+    prm.splitk_cnt =
+        reinterpret_cast<int32_t*>(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset);
+  }
   if (p->pair && !p->static_schedule && !p->one_tile_per_cta) {
     // the tile counter sits in the plan's status block, 64 bytes past the status word
     prm.tile_counter = p->d_status + 16;
@@ -547,15 +637,13 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
     case GF_OPT_TILE_N:
       if (value != 0 && value != 128 && value != 256) return fail(GF_ERR_INVALID_VALUE);
       p->forced_tile_n = static_cast<int>(value);
-      plan_tiles(p);
-      return GF_OK;
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_KERNEL:
       if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
       if (value >= 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
       if (value == 3 && gf::epi_dual(p->epi)) return fail(GF_ERR_UNSUPPORTED);
       p->forced_kernel = static_cast<int>(value);
-      plan_tiles(p);
-      return GF_OK;
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_L2_HINTS:
       if (value < 0 || value > 22 || value % 10 > 2 || value / 10 > 2)
         return fail(GF_ERR_INVALID_VALUE);
@@ -566,13 +654,15 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
       p->one_tile_per_cta = value == 1 ? 1 : 0;
       p->static_schedule = value == 3 ? 1 : 0;
-      plan_tiles(p);
-      return GF_OK;
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_GROUP_M:
       if (value < 0 || value > 4096) return fail(GF_ERR_INVALID_VALUE);
       p->forced_group_m = static_cast<int>(value);
-      plan_tiles(p);
-      return GF_OK;
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
+    case GF_OPT_SPLIT_K:
+      if (value < 0 || value > 64) return fail(GF_ERR_INVALID_VALUE);
+      p->forced_split = static_cast<int>(value);
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_FAULT_DROP_LOAD:
       if (value < 0 || value > kMaxDim) return fail(GF_ERR_INVALID_VALUE);
       p->drop_load = static_cast<int>(value);
@@ -590,13 +680,14 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   ExecArgs x = {A, B, nullptr, bias, out, aux_in, nullptr, aux_out, nullptr, bgrad};
   // candidates: {kernel (1 single, 2 pair, 3 pair with 256 x 512 tiles), tile_n, schedule,
-  // group_m}
-  struct Cand { int kernel, tile_n, schedule, group_m; };
-  const Cand cands[] = {{2, 0, 2, 8}, {2, 0, 2, 4}, {2, 0, 2, 16}, {2, 0, 3, 8},
-                        {3, 0, 2, 8}, {3, 0, 2, 16}, {3, 0, 2, 4},
-                        {1, 256, 0, 8}, {1, 128, 0, 8}, {1, 256, 0, 4}};
-  const int saved[5] = {p->forced_kernel, p->forced_tile_n, p->one_tile_per_cta,
-                        p->static_schedule, p->forced_group_m};
+  // group_m, k-split (0 the plan's choice, 1 none, else splits per tile)}
+  struct Cand { int kernel, tile_n, schedule, group_m, split; };
+  const Cand cands[] = {{2, 0, 2, 8, 0},   {2, 0, 2, 4, 0},   {2, 0, 2, 16, 0}, {2, 0, 3, 8, 0},
+                        {3, 0, 2, 8, 0},   {3, 0, 2, 16, 0},  {3, 0, 2, 4, 0},  {1, 256, 0, 8, 0},
+                        {1, 128, 0, 8, 0}, {1, 256, 0, 4, 0}, {1, 128, 0, 8, 1}, {1, 128, 0, 8, 2},
+                        {1, 128, 0, 8, 4}, {1, 128, 0, 8, 8}};
+  const int saved[6] = {p->forced_kernel, p->forced_tile_n, p->one_tile_per_cta,
+                        p->static_schedule, p->forced_group_m, p->forced_split};
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
     return fail(GF_ERR_CUDA);
@@ -611,7 +702,10 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
     p->one_tile_per_cta = 0;
     p->static_schedule = c.schedule == 3 ? 1 : 0;
     p->forced_group_m = c.group_m;
-    plan_tiles(p);
+    p->forced_split = c.split;
+    if (replan(p) != GF_OK) continue;
+    // an explicit split the tiling does not take is the same run as split 1
+    if (c.split >= 2 && p->k_splits != c.split) continue;
     gf_status s = execute_impl(p, x, st);  // warm-up, and the check of the arguments
     if (s != GF_OK) {
       st_out = s;
@@ -639,7 +733,8 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
     p->one_tile_per_cta = saved[2];
     p->static_schedule = saved[3];
     p->forced_group_m = saved[4];
-    plan_tiles(p);
+    p->forced_split = saved[5];
+    replan(p);
     return st_out != GF_OK ? fail(st_out) : fail(GF_ERR_UNSUPPORTED);
   }
   p->forced_kernel = best.kernel;
@@ -647,8 +742,8 @@ GF_API gf_status gf_matmul_autotune(gf_plan* p, const void* A, const void* B, co
   p->one_tile_per_cta = 0;
   p->static_schedule = best.schedule == 3 ? 1 : 0;
   p->forced_group_m = best.group_m;
-  plan_tiles(p);
-  return GF_OK;
+  p->forced_split = best.split;
+  return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
 }
 
 GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* tile_n,
@@ -658,7 +753,14 @@ GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* ti
   if (tile_n) *tile_n = p->tile_n;
   if (stages) *stages = p->stages;
   if (grid) *grid = p->grid;
-  if (workspace_bytes) *workspace_bytes = static_cast<int64_t>(p->partial_bytes) + 256;
+  if (workspace_bytes)
+    *workspace_bytes = static_cast<int64_t>(p->partial_bytes + p->splitk_bytes) + 256;
+  return GF_OK;
+}
+
+GF_API gf_status gf_plan_k_splits(const gf_plan* p, int32_t* k_splits) {
+  if (!p || !k_splits) return fail(GF_ERR_INVALID_VALUE);
+  *k_splits = p->k_splits;
   return GF_OK;
 }
 
@@ -699,6 +801,11 @@ GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {
     // accumulator buffer, 8 epilogue, 16 teardown drain
     if (getenv("GF_DEBUG")) fprintf(stderr, "gf: device status word 0x%x\n", word);
     if (cudaMemset(p->d_status, 0, 4) != cudaSuccess) return fail(GF_ERR_CUDA);
+    // a launch that gave up may leave split-k counters part-way
+    if (p->k_splits > 1 &&
+        cudaMemset(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset, 0,
+                   static_cast<size_t>(p->num_tiles) * 4) != cudaSuccess)
+      return fail(GF_ERR_CUDA);
     return fail(GF_ERR_DEVICE_TIMEOUT);
   }
   return GF_OK;
@@ -708,6 +815,7 @@ GF_API void gf_plan_free(gf_plan* p) {
   if (!p) return;
   cudaSetDevice(p->device);
   if (p->d_partials) cudaFree(p->d_partials);
+  if (p->d_splitk) cudaFree(p->d_splitk);
   if (p->d_status) cudaFree(p->d_status);
   free(p);
 }

@@ -248,7 +248,8 @@ typedef enum gf_option {
   GF_OPT_KERNEL = 4,
   GF_OPT_GROUP_M = 5,
   GF_OPT_L2_HINTS = 6,
-  GF_OPT_SCHEDULE = 7
+  GF_OPT_SCHEDULE = 7,
+  GF_OPT_SPLIT_K = 8
 } gf_option;
 /* GF_OPT_SCHEDULE: how persistent CTAs (or CTA pairs) walk the output tiles,
  * overlapping each tile's epilogue with the next tile's mainloop.
@@ -265,6 +266,19 @@ typedef enum gf_option {
  * (128 rows, or 256 for the CTA-pair kernel), column by column within a
  * group, so that concurrently running tiles share operand panels in L2.
  * 0: the plan's choice (8); 1..4096 otherwise. */
+/* GF_OPT_SPLIT_K: the single-CTA kernel shares the k-blocks of each output
+ * tile among this many CTAs (one B operand only; not the CTA-pair kernels).
+ * Each CTA leaves its fp32 partial sum in the plan's workspace; the last one
+ * of a tile to finish adds the partials in split order (the result does not
+ * depend on which finishes last) and runs the epilogue, so no CTA waits for
+ * another. 0: the plan's choice (a split when k has at least 16 blocks of 64
+ * and the tiles fill at most half the SMs: as many splits as the idle SMs
+ * take, at most 8 and at most sqrt(k / 128)); 1: no split; 2..64: that many
+ * (fewer when k has fewer 64-wide blocks; none when the partial sums would
+ * take more than 256 MB). The workspace grows to tiles x splits x 128 x tile_n
+ * fp32 plus one counter per tile; GF_ERR_OUT_OF_MEMORY (and no split) when it
+ * cannot be allocated. Set options only while no launch of the plan is in
+ * flight. */
 
 GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);
 
@@ -274,8 +288,8 @@ GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t val
  * through MatmulPlanPreferences; here a search over this library's own
  * kernels). Runs the planned product once per candidate (CTA-pair kernel
  * with 256- or 512-wide tiles, dynamic or static schedule and raster groups
- * of 4, 8 or 16 tile rows; single-CTA kernel with 256- or 128-wide tiles) on
- * the caller's buffers,
+ * of 4, 8 or 16 tile rows; single-CTA kernel with 256- or 128-wide tiles,
+ * and with 128-wide tiles k split 1, 2, 4 or 8 ways) on the caller's buffers,
  * `reps` timed launches each after one warm-up, synchronising `stream`, and
  * keeps the fastest in the plan. The outputs hold the result of the last
  * launch. Arguments as gf_matmul_execute; reps in 1..100.
@@ -289,6 +303,11 @@ GF_API gf_status gf_matmul_autotune(gf_plan* plan, const void* A, const void* B,
  * launch), workspace bytes. Any out-pointer may be NULL. */
 GF_API gf_status gf_plan_describe(const gf_plan* plan, int32_t* tile_m, int32_t* tile_n,
                                   int32_t* stages, int32_t* grid, int64_t* workspace_bytes);
+
+/* The number of CTAs that share the k-blocks of one output tile in the
+ * plan's current configuration (1: no split). GF_ERR_INVALID_VALUE for a
+ * NULL argument. */
+GF_API gf_status gf_plan_k_splits(const gf_plan* plan, int32_t* k_splits);
 
 /*
  * DRELU_BGRAD that allocates nothing. The pages have no counterpart: this

@@ -66,6 +66,9 @@ def test_null_plan_calls(L):
     assert L.gf_plan_set_option(None, 0, 0) == gf.GF_ERR_INVALID_VALUE
     assert L.gf_matmul_autotune(None, None, None, None, None, None, None, None, None, 3) == \
         gf.GF_ERR_INVALID_VALUE
+    ks = ctypes.c_int32(-1)
+    assert L.gf_plan_k_splits(None, ctypes.byref(ks)) == gf.GF_ERR_INVALID_VALUE
+    assert ks.value == -1
     L.gf_plan_free(None)
 
 
