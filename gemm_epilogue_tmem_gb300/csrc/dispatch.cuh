@@ -18,8 +18,17 @@ cudaError_t launch_instance(const LaunchArgs& a) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kernel<<<a.grid, kThreads, smem, a.stream>>>(*a.tmA, *a.tmB, *a.tmB2, *a.params);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.params);
 }
 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
@@ -40,13 +49,15 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
   cfg.blockDim = dim3(C::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.params);
 }
 

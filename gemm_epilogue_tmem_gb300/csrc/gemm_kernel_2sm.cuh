@@ -191,6 +191,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   cluster_sync();  // barriers of both CTAs initialised before any remote use
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  // the set-up above overlaps the previous kernel on the stream; its outputs
+  // (this kernel's inputs) are complete from here on
+  grid_dep_wait();
+  grid_dep_launch();
   bool aborted = false;
   const uint32_t tile_empty_leader = mapa_shared(tile_empty0, 0);
 

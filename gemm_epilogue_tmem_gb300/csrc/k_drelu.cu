@@ -9,6 +9,8 @@ __global__ void __launch_bounds__(256) bgrad_finalize_kernel(const float* __rest
                                                              int num_m_blocks, int N,
                                                              float* __restrict__ bgrad) {
   __shared__ float red[8][33];
+  grid_dep_wait();  // the partials of the GEMM kernel before it
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const int slice = threadIdx.x >> 5;
   const int col = blockIdx.x * 32 + lane;
@@ -28,10 +30,17 @@ __global__ void __launch_bounds__(256) bgrad_finalize_kernel(const float* __rest
 cudaError_t launch_drelu(const LaunchArgs& a) { return launch_epi<EPI_DRELU_BGRAD>(a); }
 
 cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
-                                  cudaStream_t stream) {
-  const int blocks = (n + 31) / 32;
-  bgrad_finalize_kernel<<<blocks, 256, 0, stream>>>(partial, num_m_blocks, n, bgrad);
-  return cudaGetLastError();
+                                  cudaStream_t stream, int pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + 31) / 32, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bgrad_finalize_kernel, partial, num_m_blocks, n, bgrad);
 }
 
 }  // namespace gf

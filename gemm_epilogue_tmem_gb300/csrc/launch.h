@@ -20,6 +20,7 @@ struct LaunchArgs {
   int tile_n;   // 128 or 256 (single-CTA kernel)
   int pair;     // 1: the CTA-pair kernel (256 x 256 tiles)
   int wide;     // with pair: 256 x 512 tiles (one accumulator in two halves)
+  int pdl;      // 1: programmatic dependent launch (set-up overlaps the previous kernel)
   cudaStream_t stream;
 };
 
@@ -29,7 +30,7 @@ cudaError_t launch_drelu(const LaunchArgs& a);                // EPI_DRELU_BGRAD
 cudaError_t launch_gelu(int epi, const LaunchArgs& a);        // EPI_GELU_BIAS, _AUX_BIAS, EPI_DGELU_BGRAD
 cudaError_t launch_swiglu(int epi, const LaunchArgs& a);      // EPI_SWIGLU, _SAVE, EPI_DSWIGLU
 cudaError_t launch_bgrad_finalize(const float* partial, int num_m_blocks, int n, float* bgrad,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int pdl);
 // ring depth of the kernel the plan launches (pair with tile_n 512: wide tiles)
 int stages_for(int tile_n, int pair, int epi);
 // resident CTA pairs of the pair kernel (0 if it cannot launch)

@@ -150,10 +150,12 @@ GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtyp
   la.b_mn = b_layout == GF_B_KN ? 1 : 0;
   la.tile_n = tile_n;
   la.pair = 0;
+  la.wide = 0;
+  la.pdl = 1;
   la.stream = s;
   if (gf::launch_drelu(la) != cudaSuccess) return fail(GF_ERR_CUDA);
   if (gf::launch_bgrad_finalize(partials, static_cast<int>(m_blocks), static_cast<int>(n), bgrad,
-                                s) != cudaSuccess)
+                                s, 1) != cudaSuccess)
     return fail(GF_ERR_CUDA);
   return GF_OK;
 }

@@ -413,6 +413,20 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
 }
 
 // named barrier over `count` threads (id 0 is __syncthreads)
+// Programmatic dependent launch. grid_dep_wait: wait until the grids this
+// launch depends on have completed and their memory operations are visible
+// (returns at once for a launch without such a dependency); every global
+// memory access of a kernel comes after it. grid_dep_launch: this CTA lets
+// the launch that depends on this grid begin (its CTAs start once every CTA
+// of this grid has done so or exited, and wait in grid_dep_wait).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

@@ -55,6 +55,7 @@ struct gf_plan {
   void* d_splitk;        // split-k partial sums, then the per-tile counters
   size_t splitk_bytes;   // capacity of d_splitk
   size_t splitk_cnt_offset;
+  int pdl;               // 1: launches overlap their set-up with the previous kernel
 };
 
 namespace {
@@ -360,6 +361,7 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
   // defaults, and the environment overrides of experiments (an option set
   // on the plan afterwards wins)
   p->bgrad_mode = GF_BGRAD_TWO_PASS;
+  p->pdl = 1;
   const char* env_bgrad = getenv("GF_BGRAD_MODE");
   if (env_bgrad && strcmp(env_bgrad, "atomic") == 0) p->bgrad_mode = GF_BGRAD_ATOMIC;
   p->wait_limit_ns = 2000000000ull;
@@ -536,6 +538,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   la.tile_n = p->tile_n;
   la.pair = p->pair;
   la.wide = p->wide;
+  la.pdl = p->pdl;
   la.stream = st;
 
   cudaError_t err;
@@ -556,7 +559,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   if (err != cudaSuccess) return fail(GF_ERR_CUDA);
   if (has_bgrad(e) && !atomic) {
     err = gf::launch_bgrad_finalize(p->d_partials, p->num_m_blocks, static_cast<int>(p->n),
-                                    x.bgrad, st);
+                                    x.bgrad, st, p->pdl);
     if (err != cudaSuccess) return fail(GF_ERR_CUDA);
   }
   return GF_OK;
@@ -659,6 +662,10 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
       if (value < 0 || value > 4096) return fail(GF_ERR_INVALID_VALUE);
       p->forced_group_m = static_cast<int>(value);
       return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
+    case GF_OPT_PDL:
+      if (value != 0 && value != 1) return fail(GF_ERR_INVALID_VALUE);
+      p->pdl = static_cast<int>(value);
+      return GF_OK;
     case GF_OPT_SPLIT_K:
       if (value < 0 || value > 64) return fail(GF_ERR_INVALID_VALUE);
       p->forced_split = static_cast<int>(value);

@@ -249,7 +249,8 @@ typedef enum gf_option {
   GF_OPT_GROUP_M = 5,
   GF_OPT_L2_HINTS = 6,
   GF_OPT_SCHEDULE = 7,
-  GF_OPT_SPLIT_K = 8
+  GF_OPT_SPLIT_K = 8,
+  GF_OPT_PDL = 9
 } gf_option;
 /* GF_OPT_SCHEDULE: how persistent CTAs (or CTA pairs) walk the output tiles,
  * overlapping each tile's epilogue with the next tile's mainloop.
@@ -279,6 +280,12 @@ typedef enum gf_option {
  * fp32 plus one counter per tile; GF_ERR_OUT_OF_MEMORY (and no split) when it
  * cannot be allocated. Set options only while no launch of the plan is in
  * flight. */
+/* GF_OPT_PDL: 1 (default) launches the plan's kernels as programmatic
+ * dependent launches: a kernel's launch and set-up (barriers, tensor memory,
+ * descriptor prefetch) overlap the end of the kernel before it on the stream,
+ * and it touches global memory only once that kernel has completed and its
+ * writes are visible, so results are the same as with 0 (plain stream
+ * order). */
 
 GF_API gf_status gf_plan_set_option(gf_plan* plan, gf_option option, int64_t value);
 
