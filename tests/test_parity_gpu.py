@@ -311,6 +311,58 @@ def test_one_fused_launch():
     bwd.free()
 
 
+def test_dependent_launch_changes_nothing():
+    """Programmatic dependent launch (GF_OPT_PDL, the default) against plain
+    stream order: the tiny MLP step (forward GEMM, backward GEMM, bias-gradient
+    finalize back to back, every kernel reading what the one before wrote),
+    directly and captured in a CUDA graph, gives the same bits."""
+    w = synth.MLP_TINY
+    T = {k: to_dev(synth.normal(v.shape, w.dtype, 3, v.tensor_id, v.sigma), 0)
+         for k, v in w.tensors.items()}
+    M, K = w.tensors["X"].shape
+    N = w.tensors["W1"].shape[1]
+    K2 = w.tensors["dY"].shape[1]
+    results = {}
+    for pdl in (0, 1):
+        fwd = gf.gf_matmul_plan(M, N, K, 0, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+        bwd = gf.gf_matmul_plan_ex(M, N, K2, 0, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                   gf.GF_B_NK)
+        for p in (fwd, bwd):
+            gf.gf_plan_set_option(p, gf.GF_OPT_PDL, pdl)
+        Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        aux = torch.empty(((M + 31) // 32, N), dtype=torch.int32, device="cuda")
+        G = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        bg = torch.empty(N, dtype=torch.float32, device="cuda")
+
+        def step(s=None):
+            for _ in range(5):
+                gf.gf_matmul_execute(fwd, T["X"], T["W1"], bias=T["b1"], out=Y, aux_out=aux,
+                                     stream=s)
+                gf.gf_matmul_execute(bwd, T["dY"], T["W2"], out=G, aux_in=aux, bgrad=bg,
+                                     stream=s)
+
+        step()
+        torch.cuda.synchronize()
+        direct = [t.clone() for t in (Y, aux, G, bg)]
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                step(s)
+        for t in (Y, aux, G, bg):
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert gf.gf_plan_status(fwd) == gf.GF_OK and gf.gf_plan_status(bwd) == gf.GF_OK
+        results[pdl] = direct + [t.clone() for t in (Y, aux, G, bg)]
+        fwd.free()
+        bwd.free()
+    for a, b in zip(results[0], results[1]):
+        assert torch.equal(a, b)
+    for a, b in zip(results[1][:4], results[1][4:]):
+        assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------- CTA-pair kernel
 PAIR_SHAPES = [
     (256, 256, 64),     # one pair tile
