@@ -264,7 +264,55 @@ __device__ __forceinline__ void prefetch_side(const GemmParams& p, int row0w, in
 // (store_rows32_staged), else straight from registers. SIDE: the column bias
 // (T) or this warp's mask words (uint32) of columns n0.. were prefetched into
 // shared memory at `side` (prefetch_side), and are read from there.
-template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false>
+// dSwiGLU side-input ring: per epilogue warp, slots of one 32-column chunk's
+// saved g (2 KB: 32 rows x 64 bytes) and u (2 KB), filled by asynchronous
+// copies several chunks ahead of the drain (and before the accumulator is
+// ready), in the staging buffer's layout (16-byte piece pc of row r at
+// r * 64 + ((pc ^ (r / 2 % 4)) * 16)).
+constexpr uint32_t kSideSlotBytes = 4096;
+
+// Issue (without committing) the copies of one chunk into `slot`: lane l
+// copies 16 bytes of rows 8 g + l / 4 (g = 0..3) at column col0 + 8 (l % 4),
+// of g and of u; rows at or past M and columns at or past N read nothing and
+// leave zeros.
+template <typename T>
+__device__ __forceinline__ void side_ring_issue(const GemmParams& p, int row0w, int col0,
+                                                uint32_t lane, uint32_t slot) {
+  const uint32_t pc = lane & 3u;
+  const int col = col0 + 8 * (int)pc;
+#pragma unroll
+  for (int in = 0; in < 2; ++in) {
+    const T* base = reinterpret_cast<const T*>(in == 0 ? p.aux_in : p.aux_in2);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint32_t r = 8u * g + (lane >> 2);
+      const int row = row0w + (int)r;
+      const bool ok = row < p.M && col < p.N;
+      cp_async_16(slot + 2048u * in + r * 64u + ((pc ^ ((r >> 1) & 3u)) << 4),
+                  ok ? static_cast<const void*>(base + (size_t)row * p.N + col)
+                     : static_cast<const void*>(base),
+                  ok ? 16u : 0u);
+    }
+  }
+}
+
+// The first `SRING` chunks of a drain over columns n0.. (one commit group per
+// slot, empty past N), issued before the accumulator is ready.
+template <typename T, int SRING>
+__device__ __forceinline__ void side_ring_prefetch(const GemmParams& p, int row0w, int n0,
+                                                   int nch, uint32_t lane, uint32_t ring) {
+#pragma unroll
+  for (int s = 0; s < SRING; ++s) {
+    if (s < nch) side_ring_issue<T>(p, row0w, n0 + 32 * s, lane, ring + kSideSlotBytes * s);
+    cp_async_commit();
+  }
+}
+
+// SRING > 0 (dSwiGLU with the staging buffer): the side inputs come from
+// this warp's ring of SRING chunk slots at `side`, whose first SRING chunks
+// side_ring_prefetch has issued; the drain keeps SRING chunks in flight.
+template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false,
+          int SRING = 0>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red,
                                                uint32_t stg = 0, uint32_t side = 0) {
@@ -289,7 +337,12 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   T* out = reinterpret_cast<T*>(p.out);
   const bool has_acc = p.num_k_blocks > 0;
   const int nch = min(BN / 32, (p.N - n0 + 31) / 32);  // chunks with columns below N
-  if (nch <= 0) return;
+  constexpr bool kRing = SRING > 0;
+  static_assert(!kRing || (STG && EPI == EPI_DSWIGLU), "side ring: dSwiGLU with staging");
+  if (nch <= 0) {
+    if constexpr (kRing) cp_async_wait_all();
+    return;
+  }
 
   // the saved 16-bit activations are read coalesced when the staging buffer
   // is there: lane l loads 16 bytes of row 8g + l/4 (4 lanes per 64-byte row
@@ -355,7 +408,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
     tmem_ld_32x32b_x32(t_row, ra);
     if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN, rb);
   }
-  load_side(n0, sd);
+  if constexpr (!kRing) load_side(n0, sd);
 
 #pragma unroll 1
   for (int c = 0; c < nch; ++c) {
@@ -380,7 +433,22 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     }
     uint4 cur[kSideN];
-    if constexpr (kCoalesced) {
+    if constexpr (kRing) {
+      // this chunk's slot is complete once at most SRING - 1 groups are pending
+      cp_async_wait_group<SRING - 1>();
+      __syncwarp();
+      const uint32_t slot = side + kSideSlotBytes * (uint32_t)(c % SRING);
+      const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+      for (int in = 0; in < 2; ++in) {
+#pragma unroll
+        for (uint32_t pc = 0; pc < 4; ++pc)
+          cur[4 * in + pc] = ld_shared_v4(slot + 2048u * in + lane * 64u + ((pc ^ sw) << 4));
+      }
+      __syncwarp();  // every lane has read the slot: refill it
+      if (c + SRING < nch) side_ring_issue<T>(p, row0w, col0 + 32 * SRING, lane, slot);
+      cp_async_commit();
+    } else if constexpr (kCoalesced) {
       // through the staging buffer: rows as loaded -> this lane's row
 #pragma unroll
       for (int in = 0; in < (EPI == EPI_DSWIGLU ? 2 : 1); ++in) {
@@ -407,7 +475,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
         tmem_ld_32x32b_x32(t_row + 32u * (c + 1), ra);
         if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * (c + 1), rb);
       }
-      load_side(col0 + 32, sd);
+      if constexpr (!kRing) load_side(col0 + 32, sd);
     }
 
     if constexpr (kDual) {

@@ -59,11 +59,20 @@ GF_HD constexpr bool pair_stg(int epi, bool wide) {
          epi == EPI_DGELU_BGRAD;
 }
 
+// Chunk slots of the dSwiGLU side-input ring per epilogue warp (256 x 256
+// tiles): the saved g and u of three 32-column chunks in flight ahead of the
+// drain, which is otherwise bound by the latency of those reads.
+GF_HD constexpr int pair_side_ring(int epi, bool wide) {
+  return !wide && epi == EPI_DSWIGLU ? 3 : 0;
+}
+
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
 // side in one accumulator); RED = the epilog reduces a bias gradient and
 // needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only); EPI8 =
-// eight epilogue warps (pair_epi8).
-template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE, bool STG = WIDE>
+// eight epilogue warps (pair_epi8); SRING = side-input ring slots per
+// epilogue warp (pair_side_ring).
+template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE, bool STG = WIDE,
+          int SRING = 0>
 struct PairCfg {
   static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
   static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
@@ -87,7 +96,10 @@ struct PairCfg {
   // exposed, so its stores go out as 64-byte row segments) and a 1 KB buffer
   // of the tile's prefetched side inputs (column bias or mask words of its
   // 2 x 128 columns)
-  static constexpr int kStgBytes = WIDE ? kEpiWarps * (2048 + 1024) : (STG ? kEpiWarps * 2048 : 0);
+  // (+ the side-input ring of SRING 4 KB chunk slots per warp)
+  static constexpr int kStgBytes =
+      WIDE ? kEpiWarps * (2048 + 1024)
+           : (STG ? kEpiWarps * (2048 + SRING * static_cast<int>(kSideSlotBytes)) : 0);
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes + kStgBytes;
@@ -115,13 +127,16 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
 __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
-                                          pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE)>::kThreads,
+                                          pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
+                                          pair_side_ring(EPI, WIDE)>::kThreads,
                                   1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
-  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE)>;
+  using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
+                    pair_side_ring(EPI, WIDE)>;
+  constexpr int kRing = pair_side_ring(EPI, WIDE);
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -154,6 +169,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
 
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
+  // dSwiGLU: an epilogue warp's side-input ring (kRing slots) after the staging buffers
+  const uint32_t sring = side0 + kRing * kSideSlotBytes * (uint32_t)(warp >= 2 ? warp - 2 : 0);
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int cluster_id = blockIdx.x >> 1;
@@ -498,6 +515,9 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + c_sub, lane, side);
         prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + 256 + c_sub, lane, side + kSideHalf);
       }
+      if constexpr (kRing > 0)  // the first chunks' saved g and u, under the mainloop
+        side_ring_prefetch<T, kRing>(p, row0 + 32 * q, n0, min(BN / 32, (p.N - n0 + 31) / 32),
+                                     lane, sring);
       const int buf = WIDE ? 0 : (it & 1);
       const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
       ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
@@ -543,14 +563,15 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       } else {
         constexpr bool kStg = pair_stg(EPI, false);
-        epilogue_drain<EPI, T, BN, BN, kStg>(p, t_row, row0, n0, q, lane, red,
-                                             stg0 + 2048u * (uint32_t)(warp - 2));
+        epilogue_drain<EPI, T, BN, BN, kStg, false, kRing>(
+            p, t_row, row0, n0, q, lane, red, stg0 + 2048u * (uint32_t)(warp - 2), sring);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       }
       if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN, NT>(p, red, ep_tid, n0, row0 / kBM);
     }
+    if constexpr (kRing > 0) cp_async_wait_all();  // no copy lands after the CTA is gone
   }
 
   // a CTA that gave up may still have loads in flight towards its shared

@@ -12,6 +12,8 @@ int stages_for(int tile_n, int pair, int epi) {
   if (epi_dual(epi) && pair)
     return pair_stg(epi, false) ? PairCfg<2, false, false, false, true>::kStages
                                 : PairCfg<2, false>::kStages;
+  if (pair && tile_n != 512 && pair_side_ring(epi, false) > 0)
+    return PairCfg<1, false, false, false, true, pair_side_ring(EPI_DSWIGLU, false)>::kStages;
   if (pair && tile_n != 512 && pair_stg(epi, false))
     return red ? PairCfg<1, true, false, false, true>::kStages
                : PairCfg<1, false, false, false, true>::kStages;
