@@ -2,8 +2,9 @@
 N and K multiples of 8, from tiny to several tiles with ragged tails), every
 gf_matmul epilog, fp16 and bf16, both B layouts, both bias axes, every kernel
 form (the plan's choice, single CTA at both tile widths, CTA pair, wide pair),
-k split or not, bias-gradient mode, and dependent launch on or off. The cases
-are drawn once from a fixed seed, so every run checks the same ones."""
+k split or not, bias-gradient mode, and dependent launch on or off; and the
+SwiGLU entry points the same way. The cases are drawn once from a fixed seed,
+so every run checks the same ones."""
 import numpy as np
 import pytest
 
@@ -122,3 +123,61 @@ def test_random_problem(c):
         dz_o, bgrad_o, _ = oracle.dgelu_bgrad(A, B, aux_h, d, layout)
     assert_close(to_host_f32(out), oracle.decode(dz_o, d), what="dZ")
     assert_close(bgrad.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
+
+
+def _swiglu_cases(n=40, seed=2025):
+    r = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        M = int(r.choice([1, 33, 129, 257]) if r.random() < 0.3 else r.integers(1, 900))
+        out.append(dict(i=i, M=M, I=8 * int(r.integers(1, 100)), H=8 * int(r.integers(1, 100)),
+                        dtype=int(r.integers(0, 2)), backward=bool(r.integers(0, 2)),
+                        save=bool(r.integers(0, 2)), kernel=int(r.choice([0, 1, 2, 3])),
+                        pdl=int(r.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("c", _swiglu_cases(),
+                         ids=lambda c: (f"{c['i']}-{c['M']}x{c['I']}x{c['H']}-d{c['dtype']}"
+                                        f"-{'bwd' if c['backward'] else 'fwd'}-k{c['kernel']}"))
+def test_random_swiglu(c):
+    """The gate+up forward (saving g and u or not) and the dSwiGLU backward
+    on random shapes, kernel forms (the wide pair only for the backward,
+    which has one B operand) and launch modes."""
+    M, I, H, d = c["M"], c["I"], c["H"], c["dtype"]
+    seed = 300 + c["i"]
+    tdt = torch_dtype(d)
+    if not c["backward"]:
+        x = synth.normal((M, H), d, seed, synth.TID_A, 1.0)
+        Wg = synth.normal((I, H), d, seed, synth.TID_WG, 1 / np.sqrt(H))
+        Wu = synth.normal((I, H), d, seed, synth.TID_WU, 1 / np.sqrt(H))
+        plan = gf.gf_swiglu_plan(M, I, H, d, save_gu=c["save"])
+        if c["kernel"] in (1, 2):
+            gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, c["kernel"])
+        gf.gf_plan_set_option(plan, gf.GF_OPT_PDL, c["pdl"])
+        h, g, u = (torch.empty((M, I), dtype=tdt, device="cuda") for _ in range(3))
+        gf.gf_swiglu_execute(plan, to_dev(x, d), to_dev(Wg, d), to_dev(Wu, d), h,
+                             g if c["save"] else None, u if c["save"] else None)
+        assert gf.gf_plan_status(plan) == gf.GF_OK
+        plan.free()
+        h_o, g_o, u_o, _, _ = oracle.swiglu_forward(x, Wg, Wu, d)
+        assert_close(to_host_f32(h), oracle.decode(h_o, d), what="h")
+        if c["save"]:
+            assert_close(to_host_f32(g), oracle.decode(g_o, d), what="saved g")
+            assert_close(to_host_f32(u), oracle.decode(u_o, d), what="saved u")
+        return
+    dout = synth.normal((M, H), d, seed, synth.TID_DOUT, 1.0)
+    Wd = synth.normal((H, I), d, seed, synth.TID_WD, 1 / np.sqrt(H))
+    g = synth.normal((M, I), d, seed, synth.TID_G_SAVED, 2.0)
+    u = synth.normal((M, I), d, seed, synth.TID_U_SAVED, 1.0)
+    plan = gf.gf_dswiglu_plan(M, I, H, d)
+    if c["kernel"]:
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, c["kernel"])
+    gf.gf_plan_set_option(plan, gf.GF_OPT_PDL, c["pdl"])
+    dg, du = (torch.empty((M, I), dtype=tdt, device="cuda") for _ in range(2))
+    gf.gf_dswiglu_execute(plan, to_dev(dout, d), to_dev(Wd, d), to_dev(g, d), to_dev(u, d), dg, du)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    dg_o, du_o, _ = oracle.dswiglu_backward(dout, Wd, g, u, d)
+    assert_close(to_host_f32(dg), oracle.decode(dg_o, d), what="d_gate")
+    assert_close(to_host_f32(du), oracle.decode(du_o, d), what="d_up")
