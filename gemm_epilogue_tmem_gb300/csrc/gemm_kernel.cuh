@@ -612,7 +612,8 @@ __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float*
 template <int BN>
 __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_row, int t, int s,
                                               int ks, int q, uint32_t lane, int ep_tid,
-                                              volatile int* last_flag) {
+                                              volatile int* last_flag, uint32_t ring,
+                                              uint32_t ring_bytes) {
   constexpr int kPart = kBM * BN / 4;  // float4 pieces of one partial
   const int row = 32 * q + static_cast<int>(lane);
   float4* tile_ws = reinterpret_cast<float4*>(p.splitk_ws) + static_cast<size_t>(t) * ks * kPart;
@@ -639,6 +640,27 @@ __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_ro
   named_bar_sync(1, 128);
   if (*last_flag == 0) return false;
   __threadfence();
+  // When the operand ring is idle (`ring_bytes` > 0: this CTA's last unit,
+  // every stage consumed) and holds the other splits' partials, they come in
+  // by asynchronous copies all issued at once -- piece pc of this row from
+  // the j-th other split at ((j * BN / 4 + pc) * 128 + row) * 16 -- instead
+  // of a few loads in flight per thread.
+  const bool staged = ring_bytes >= static_cast<uint32_t>((ks - 1) * kPart * 16);
+  if (staged) {
+    int j = 0;
+#pragma unroll 1
+    for (int sp = 0; sp < ks; ++sp) {
+      if (sp == s) continue;
+      const float4* src = tile_ws + static_cast<size_t>(sp) * kPart + row;
+#pragma unroll 8
+      for (int pc = 0; pc < BN / 4; ++pc)
+        cp_async_16(ring + static_cast<uint32_t>(((j * (BN / 4) + pc) * kBM + row) * 16),
+                    src + pc * kBM, 16u);
+      ++j;
+    }
+    cp_async_commit();
+    cp_async_wait_all();  // each thread reads back only what it copied itself
+  }
 #pragma unroll 1
   for (int c = 0; c < BN; c += 32) {
     // this CTA's own partial is still in its accumulator
@@ -647,43 +669,67 @@ __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_ro
     tmem_ld_wait_tied(own);
     const float4* src = tile_ws + (c / 4) * kBM + row;
     float acc[32];
+    if (staged) {
 #pragma unroll 1
-    for (int sp = 0; sp < ks; sp += 2) {
-      // two splits' pieces in flight at once; a split's own piece from TMEM
-      float4 x[8], y[8];
-      const float4* a = src + static_cast<size_t>(sp) * kPart;
-      const float4* b = a + kPart;
-      const bool has_b = sp + 1 < ks;
+      for (int sp = 0; sp < ks; ++sp) {
+        float x[32];
+        if (sp == s) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        x[j] = sp == s ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
-                                     __uint_as_float(own[4 * j + 2]),
-                                     __uint_as_float(own[4 * j + 3]))
-                       : __ldcg(a + j * kBM);
-        y[j] = !has_b ? make_float4(0.f, 0.f, 0.f, 0.f)
-               : sp + 1 == s
-                   ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
-                                 __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]))
-                   : __ldcg(b + j * kBM);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (sp == 0) {
-          acc[4 * j] = x[j].x;
-          acc[4 * j + 1] = x[j].y;
-          acc[4 * j + 2] = x[j].z;
-          acc[4 * j + 3] = x[j].w;
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(own[i]);
         } else {
-          acc[4 * j] += x[j].x;
-          acc[4 * j + 1] += x[j].y;
-          acc[4 * j + 2] += x[j].z;
-          acc[4 * j + 3] += x[j].w;
+          const int j = sp < s ? sp : sp - 1;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 w = ld_shared_v4(
+                ring + static_cast<uint32_t>(((j * (BN / 4) + c / 4 + k) * kBM + row) * 16));
+            x[4 * k] = __uint_as_float(w.x);
+            x[4 * k + 1] = __uint_as_float(w.y);
+            x[4 * k + 2] = __uint_as_float(w.z);
+            x[4 * k + 3] = __uint_as_float(w.w);
+          }
         }
-        if (has_b) {
-          acc[4 * j] += y[j].x;
-          acc[4 * j + 1] += y[j].y;
-          acc[4 * j + 2] += y[j].z;
-          acc[4 * j + 3] += y[j].w;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = sp == 0 ? x[i] : acc[i] + x[i];
+      }
+    } else {
+#pragma unroll 1
+      for (int sp = 0; sp < ks; sp += 2) {
+        // two splits' pieces in flight at once; a split's own piece from TMEM
+        float4 x[8], y[8];
+        const float4* a = src + static_cast<size_t>(sp) * kPart;
+        const float4* b = a + kPart;
+        const bool has_b = sp + 1 < ks;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          x[j] = sp == s ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                       __uint_as_float(own[4 * j + 2]),
+                                       __uint_as_float(own[4 * j + 3]))
+                         : __ldcg(a + j * kBM);
+          y[j] = !has_b ? make_float4(0.f, 0.f, 0.f, 0.f)
+                 : sp + 1 == s
+                     ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),
+                                   __uint_as_float(own[4 * j + 2]), __uint_as_float(own[4 * j + 3]))
+                     : __ldcg(b + j * kBM);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (sp == 0) {
+            acc[4 * j] = x[j].x;
+            acc[4 * j + 1] = x[j].y;
+            acc[4 * j + 2] = x[j].z;
+            acc[4 * j + 3] = x[j].w;
+          } else {
+            acc[4 * j] += x[j].x;
+            acc[4 * j + 1] += x[j].y;
+            acc[4 * j + 2] += x[j].z;
+            acc[4 * j + 3] += x[j].w;
+          }
+          if (has_b) {
+            acc[4 * j] += y[j].x;
+            acc[4 * j + 1] += y[j].y;
+            acc[4 * j + 2] += y[j].z;
+            acc[4 * j + 3] += y[j].w;
+          }
         }
       }
     }
@@ -912,7 +958,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
 
-      if (ks > 1 && !splitk_reduce<BN>(p, t_row, t, u - t * ks, ks, q, lane, ep_tid, last_flag)) {
+      // the operand ring is idle once this CTA's last unit has been multiplied
+      const uint32_t ring_bytes =
+          u + (int)gridDim.x >= units ? (uint32_t)(S * (C::kABytes + C::kStageBBytes)) : 0u;
+      if (ks > 1 && !splitk_reduce<BN>(p, t_row, t, u - t * ks, ks, q, lane, ep_tid, last_flag,
+                                       sA, ring_bytes)) {
         // a partial sum, handed over through the workspace: buffer free again
         tc_fence_before();
         __syncwarp();
