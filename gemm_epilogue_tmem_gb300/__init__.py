@@ -23,7 +23,7 @@ __all__ = [
     "GF_BIAS_COL", "GF_BIAS_ROW", "GF_B_KN", "GF_B_NK", "GF_BGRAD_TWO_PASS", "GF_BGRAD_ATOMIC",
     "GF_OPT_BGRAD_MODE", "GF_OPT_WAIT_LIMIT_US", "GF_OPT_TILE_N", "GF_OPT_FAULT_DROP_LOAD",
     "GF_OPT_KERNEL", "GF_OPT_GROUP_M", "GF_OPT_L2_HINTS", "GF_OPT_SCHEDULE", "GF_OPT_SPLIT_K",
-    "GF_OPT_PDL",
+    "GF_OPT_PDL", "GF_OPT_RASTER",
     "GfError", "Plan", "build", "lib", "gf_matmul_plan", "gf_matmul_plan_ex",
     "gf_matmul_execute", "gf_plan_status", "gf_plan_set_option", "gf_plan_describe",
     "gf_plan_free", "gf_status_string", "gf_last_error", "gf_drelu_bgrad_noalloc",
@@ -47,7 +47,7 @@ GF_BGRAD_TWO_PASS, GF_BGRAD_ATOMIC = 0, 1
 # gf_option
 GF_OPT_BGRAD_MODE, GF_OPT_WAIT_LIMIT_US, GF_OPT_TILE_N, GF_OPT_FAULT_DROP_LOAD = 0, 1, 2, 3
 GF_OPT_KERNEL, GF_OPT_GROUP_M, GF_OPT_L2_HINTS, GF_OPT_SCHEDULE = 4, 5, 6, 7
-GF_OPT_SPLIT_K, GF_OPT_PDL = 8, 9
+GF_OPT_SPLIT_K, GF_OPT_PDL, GF_OPT_RASTER = 8, 9, 10
 # fp32 partial sums the allocation-free DRELU_BGRAD entry point can hold
 GF_NOALLOC_MAX_PARTIALS = 2097152
 

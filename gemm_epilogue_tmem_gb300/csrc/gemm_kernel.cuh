@@ -203,6 +203,16 @@ __device__ __forceinline__ void emit_row32(T* base, int M, int N, int row0w, int
 // Tile t -> (m block, n block): groups of group_m row blocks are swept
 // column by column so that CTAs running together share A and B in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+  if (p.raster_n) {  // groups of group_m column blocks, columns fastest within a group
+    const int group_size = p.group_m * p.num_m_blocks;
+    const int group = t / group_size;
+    const int first_n = group * p.group_m;
+    const int gn = min(p.num_n_blocks - first_n, p.group_m);
+    const int r = t - group * group_size;
+    nb = first_n + r % gn;
+    mb = r / gn;
+    return;
+  }
   const int group_size = p.group_m * p.num_n_blocks;
   const int group = t / group_size;
   const int first_m = group * p.group_m;

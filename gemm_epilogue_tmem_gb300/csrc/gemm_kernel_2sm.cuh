@@ -112,6 +112,16 @@ constexpr int kTileRing = 4;  // tile indices in flight between the roles (dynam
 // Pair tile t -> (256-row block, 256-column block), grouped like tile_coords.
 __device__ __forceinline__ void pair_tile_coords(const GemmParams& p, int t, int& mb2, int& nb) {
   const int num_m2 = (p.num_m_blocks + 1) / 2;
+  if (p.raster_n) {  // groups of group_m column blocks, columns fastest within a group
+    const int group_size = p.group_m * num_m2;
+    const int group = t / group_size;
+    const int first_n = group * p.group_m;
+    const int gn = min(p.num_n_blocks - first_n, p.group_m);
+    const int r = t - group * group_size;
+    nb = first_n + r % gn;
+    mb2 = r / gn;
+    return;
+  }
   const int group_size = p.group_m * p.num_n_blocks;
   const int group = t / group_size;
   const int first_m = group * p.group_m;

@@ -60,6 +60,7 @@ enum : int {
 struct GemmParams {
   int32_t M, N, K;
   int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+  int32_t raster_n;      // 0: groups of group_m row blocks; 1: groups of group_m column blocks
   int32_t bias_axis;     // 0: bias[N] per column, 1: bias[M] per row
   int32_t bgrad_atomic;  // DRELU_BGRAD: 1 = atomicAdd into bgrad[N], 0 = partials
   const void* bias;

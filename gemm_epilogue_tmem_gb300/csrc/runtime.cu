@@ -33,7 +33,9 @@ struct gf_plan {
   int tile_n;
   int forced_tile_n;
   int forced_kernel;     // 0 auto, 1 single CTA, 2 CTA pair, 3 CTA pair with 256 x 512 tiles
-  int forced_group_m;    // 0 auto, else row blocks per raster group
+  int forced_group_m;    // 0 auto, else row (or column) blocks per raster group
+  int forced_raster;     // 0 auto, 1 groups of row blocks, 2 groups of column blocks
+  int raster_n;          // 1: raster groups of column blocks (B panels stay in L2)
   int l2_hint_a, l2_hint_b;  // L2 eviction policy of the A / B loads (0 none, 1 first, 2 last)
   int one_tile_per_cta;  // 1: grid of one tile per CTA (pair); the hardware orders the tiles
   int static_schedule;   // 1: persistent CTA pairs walk every gridDim-th tile (default: counter)
@@ -161,6 +163,7 @@ void plan_tiles(gf_plan* p) {
   const int64_t mblocks = (p->m + kBM - 1) / kBM;
   p->num_m_blocks = static_cast<int>(mblocks);
   p->num_k_blocks = static_cast<int>((p->k + 63) / 64);
+  p->raster_n = p->forced_raster == 2 ? 1 : 0;
   p->group_m = p->forced_group_m > 0 ? p->forced_group_m : 8;
   p->k_splits = 1;
   p->kb_per_split = p->num_k_blocks;
@@ -191,6 +194,13 @@ void plan_tiles(gf_plan* p) {
            tiles256 >= p->max_pair_clusters;
   p->pair = pair ? 1 : 0;
   p->wide = pair && wide ? 1 : 0;
+  // wide tiles: groups of 4 column blocks (4 B panels of 512 columns stay in
+  // L2 while A streams) measured 0.3-0.7 % faster at the power cap than
+  // groups of 8 row blocks on the large linear pair
+  if (p->wide && p->forced_raster == 0) {
+    p->raster_n = 1;
+    if (p->forced_group_m == 0) p->group_m = 4;
+  }
   if (pair) {
     p->tile_n = pair_n;
     p->stages = gf::stages_for(pair_n, 1, p->epi);
@@ -492,6 +502,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.num_k_blocks = p->num_k_blocks;
   prm.num_tiles = p->num_tiles;
   prm.group_m = p->group_m;
+  prm.raster_n = p->raster_n;
   prm.bias_axis = p->bias_axis == GF_BIAS_ROW ? 1 : 0;
   prm.bias = x.bias;
   prm.out = x.out;
@@ -661,6 +672,10 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
     case GF_OPT_GROUP_M:
       if (value < 0 || value > 4096) return fail(GF_ERR_INVALID_VALUE);
       p->forced_group_m = static_cast<int>(value);
+      return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
+    case GF_OPT_RASTER:
+      if (value < 0 || value > 2) return fail(GF_ERR_INVALID_VALUE);
+      p->forced_raster = static_cast<int>(value);
       return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_PDL:
       if (value != 0 && value != 1) return fail(GF_ERR_INVALID_VALUE);

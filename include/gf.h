@@ -250,7 +250,8 @@ typedef enum gf_option {
   GF_OPT_L2_HINTS = 6,
   GF_OPT_SCHEDULE = 7,
   GF_OPT_SPLIT_K = 8,
-  GF_OPT_PDL = 9
+  GF_OPT_PDL = 9,
+  GF_OPT_RASTER = 10
 } gf_option;
 /* GF_OPT_SCHEDULE: how persistent CTAs (or CTA pairs) walk the output tiles,
  * overlapping each tile's epilogue with the next tile's mainloop.
@@ -264,9 +265,10 @@ typedef enum gf_option {
  * a (for A) and b (for B) each 0 = no hint, 1 = evict first (streamed),
  * 2 = evict last (re-read by the tiles that follow). */
 /* GF_OPT_GROUP_M: output tiles are visited in groups of this many row blocks
- * (128 rows, or 256 for the CTA-pair kernel), column by column within a
- * group, so that concurrently running tiles share operand panels in L2.
- * 0: the plan's choice (8); 1..4096 otherwise. */
+ * (128 rows, or 256 for the CTA-pair kernel) -- or column blocks, see
+ * GF_OPT_RASTER -- so that concurrently running tiles share operand panels
+ * in L2. 0: the plan's choice (8, or 4 column blocks for the 256 x 512
+ * tiles); 1..4096 otherwise. */
 /* GF_OPT_SPLIT_K: the single-CTA kernel shares the k-blocks of each output
  * tile among this many CTAs (one B operand only; not the CTA-pair kernels).
  * Each CTA leaves its fp32 partial sum in the plan's workspace; the last one
@@ -280,6 +282,12 @@ typedef enum gf_option {
  * fp32 plus one counter per tile; GF_ERR_OUT_OF_MEMORY (and no split) when it
  * cannot be allocated. Set options only while no launch of the plan is in
  * flight. */
+/* GF_OPT_RASTER: the order of the output tiles. 1: raster groups of
+ * GF_OPT_GROUP_M row blocks, column by column within a group (the group's
+ * A panels stay in L2 while B streams through); 2: groups of GF_OPT_GROUP_M
+ * column blocks, row by row within a group (B panels stay in L2); 0 (default)
+ * the plan's choice: 2 with groups of 4 for the 256 x 512 tiles, else 1 with
+ * groups of 8. Results are the same in every order. */
 /* GF_OPT_PDL: 1 (default) launches the plan's kernels as programmatic
  * dependent launches: a kernel's launch and set-up (barriers, tensor memory,
  * descriptor prefetch) overlap the end of the kernel before it on the stream,

@@ -150,3 +150,40 @@ def test_autotune_rejects_bad_reps():
         with pytest.raises(gf.GfError):
             gf.gf_matmul_autotune(plan, a, w, out=o, reps=reps)
     plan.free()
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3])
+def test_raster_orders_give_the_same_bits(data, kernel):
+    """Groups of row blocks or of column blocks (GF_OPT_RASTER 1 / 2), of
+    several sizes, visit the same tiles in another order: the forward output,
+    its mask and the backward's dZ and two-pass bias gradient are identical
+    bit for bit, and match the oracle."""
+    X, W, Wt, b, words, y_o, z_o, dz_o, bgrad_o = data
+    Xd, Wd, Wtd, bd, wd = to_dev(X, 0), to_dev(W, 0), to_dev(Wt, 0), to_dev(b, 0), to_dev(words, 0)
+    results = []
+    for raster, group in ((0, 0), (1, 8), (2, 4), (2, 1), (2, 3)):
+        fwd = gf.gf_matmul_plan(M, N, K, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+        bwd = gf.gf_matmul_plan_ex(M, N, K, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                   gf.GF_B_NK)
+        for p in (fwd, bwd):
+            gf.gf_plan_set_option(p, gf.GF_OPT_KERNEL, kernel)
+            gf.gf_plan_set_option(p, gf.GF_OPT_RASTER, raster)
+            gf.gf_plan_set_option(p, gf.GF_OPT_GROUP_M, group)
+        y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        aux = torch.empty(((M + 31) // 32, N), dtype=torch.int32, device="cuda")
+        dz = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        bg = torch.empty((N,), dtype=torch.float32, device="cuda")
+        gf.gf_matmul_execute(fwd, Xd, Wd, bias=bd, out=y, aux_out=aux)
+        gf.gf_matmul_execute(bwd, Xd, Wtd, out=dz, aux_in=wd, bgrad=bg)
+        assert gf.gf_plan_status(fwd) == gf.GF_OK and gf.gf_plan_status(bwd) == gf.GF_OK
+        fwd.free()
+        bwd.free()
+        results.append((y, aux, dz, bg))
+    for r in results[1:]:
+        for a, c in zip(results[0], r):
+            assert torch.equal(a, c)
+    y, aux, dz, bg = results[0]
+    assert_close(to_host_f32(y), oracle.decode(y_o, 0), what="Y")
+    assert mask_mismatch(unpack_words(to_host_words(aux), M), z_o)[0] == 0
+    assert_close(to_host_f32(dz), oracle.decode(dz_o, 0), what="dZ")
+    assert_close(bg.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
