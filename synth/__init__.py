@@ -38,6 +38,7 @@ TID_WG, TID_WU, TID_WD, TID_DOUT = 8, 9, 10, 11
 TID_PREACT = 12
 TID_G_SAVED, TID_U_SAVED = 13, 14
 TID_SAMPLE = 100
+TID_SAMPLE_COL = 101  # sampled columns (bias-gradient checks)
 
 
 def build_host(force: bool = False) -> str:
@@ -186,6 +187,13 @@ def sample_rows(M: int, count: int, seed: int) -> np.ndarray:
     """Sorted distinct rows drawn as h(t) mod M, t = 0..count-1."""
     out = np.empty(count, dtype=np.int64)
     _host_lib().synth_sample_rows(out.ctypes.data, count, M, seed, TID_SAMPLE)
+    return np.unique(out)
+
+
+def sample_cols(N: int, count: int, seed: int) -> np.ndarray:
+    """Sorted distinct columns drawn as h(t) mod N from their own stream."""
+    out = np.empty(count, dtype=np.int64)
+    _host_lib().synth_sample_rows(out.ctypes.data, count, N, seed, TID_SAMPLE_COL)
     return np.unique(out)
 
 

@@ -90,23 +90,26 @@ def test_dynamic_schedule_swiglu_and_gelu():
 
 
 def test_dynamic_schedule_wait_limit():
-    X = torch.randn((1024, 512), device="cuda").half()
-    W = torch.randn((512, 1024), device="cuda").half() / 16
-    bias = torch.zeros(1024, device="cuda").half()
-    out = torch.empty((1024, 1024), dtype=torch.float16, device="cuda")
-    plan = gf.gf_matmul_plan(1024, 1024, 512, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL)
+    Mw, Nw, Kw = 1024, 1024, 512
+    X = synth.normal((Mw, Kw), synth.F16, 33, synth.TID_A, 1.0)
+    W = synth.normal((Kw, Nw), synth.F16, 33, synth.TID_B, 1 / np.sqrt(Kw))
+    b = synth.normal((Nw,), synth.F16, 33, synth.TID_BIAS, 0.1)
+    Xd, Wd, bd = to_dev(X, 0), to_dev(W, 0), to_dev(b, 0)
+    out = torch.empty((Mw, Nw), dtype=torch.float16, device="cuda")
+    plan = gf.gf_matmul_plan(Mw, Nw, Kw, gf.GF_F16, gf.GF_EPILOG_RELU_BIAS, gf.GF_BIAS_COL)
     gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
     gf.gf_plan_set_option(plan, gf.GF_OPT_SCHEDULE, 2)
     gf.gf_plan_set_option(plan, gf.GF_OPT_WAIT_LIMIT_US, 20000)
     gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 3)
-    gf.gf_matmul_execute(plan, X, W, bias=bias, out=out)
+    gf.gf_matmul_execute(plan, Xd, Wd, bias=bd, out=out)
     assert gf.gf_plan_status(plan) == gf.GF_ERR_DEVICE_TIMEOUT
     gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 0)
-    gf.gf_matmul_execute(plan, X, W, bias=bias, out=out)
+    out.fill_(float("nan"))
+    gf.gf_matmul_execute(plan, Xd, Wd, bias=bd, out=out)
     assert gf.gf_plan_status(plan) == gf.GF_OK
-    ref = torch.relu(X.float() @ W.float())
-    assert float((out.float() - ref).abs().max() / ref.abs().max()) < 2e-2
     plan.free()
+    y_o, _ = oracle.relu_bias(X, W, b, oracle.F16)
+    assert_close(to_host_f32(out), oracle.decode(y_o, oracle.F16), what="Y after the time-out")
 
 
 @pytest.mark.parametrize("epilog", ["fwd", "bwd"])

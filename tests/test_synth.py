@@ -75,3 +75,10 @@ def test_sample_rows():
     r = synth.sample_rows(65536, 64, 0)
     assert r.size > 50 and r.min() >= 0 and r.max() < 65536
     assert np.array_equal(r, synth.sample_rows(65536, 64, 0))
+
+
+def test_sample_cols():
+    c = synth.sample_cols(16384, 64, 0)
+    assert c.size > 50 and c.min() >= 0 and c.max() < 16384
+    assert np.array_equal(c, synth.sample_cols(16384, 64, 0))
+    assert not np.array_equal(c, synth.sample_rows(16384, 64, 0))  # its own stream
