@@ -27,6 +27,7 @@ __all__ = [
     "GfError", "Plan", "build", "lib", "gf_matmul_plan", "gf_matmul_plan_ex",
     "gf_matmul_execute", "gf_plan_status", "gf_plan_set_option", "gf_plan_describe",
     "gf_plan_free", "gf_status_string", "gf_last_error", "gf_drelu_bgrad_noalloc",
+    "gf_noalloc_status",
     "gf_swiglu_plan", "gf_swiglu_execute", "gf_dswiglu_plan", "gf_dswiglu_execute",
     "GF_NOALLOC_MAX_PARTIALS",
 ]
@@ -105,6 +106,8 @@ def lib(path: str | None = None):
         L.gf_matmul_autotune.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I32]
         L.gf_drelu_bgrad_noalloc.restype = _I32
         L.gf_drelu_bgrad_noalloc.argtypes = [_I64, _I64, _I64, _I32, _I32, _P, _P, _P, _P, _P, _P]
+        L.gf_noalloc_status.restype = _I32
+        L.gf_noalloc_status.argtypes = [_P]
         _lib = L
     return _lib
 
@@ -259,3 +262,9 @@ def gf_drelu_bgrad_noalloc(m: int, n: int, k: int, dtype: int, b_layout: int, A,
                                       _ptr(aux_in), _ptr(bgrad), _stream(stream))
     if rc != GF_OK:
         raise GfError(rc, "gf_drelu_bgrad_noalloc")
+
+
+def gf_noalloc_status(stream=None) -> int:
+    """Synchronise the stream and return the status of the most recent
+    gf_drelu_bgrad_noalloc on this device (GF_OK, GF_ERR_DEVICE_TIMEOUT ...)."""
+    return int(lib().gf_noalloc_status(_stream(stream)))

@@ -854,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fb, bytes);
             tma_load(sA + stage * C::kABytes, &tmA, fb, kb * kBK, m0, p.l2_hint_a, pol_a);
             if (B_MN && p.b_mn_3d) {
-              tma_load_3d(sB + stage * C::kStageBBytes, &tmB, fb, 0, kb * kBK, n0 / 64);
+              tma_load3(sB + stage * C::kStageBBytes, &tmB, fb, 0, kb * kBK, n0 / 64,
+                        p.l2_hint_b, pol_b);
             } else if (B_MN) {
               for (int j = 0; j < nbox; ++j)
                 tma_load(sB + stage * C::kStageBBytes + j * (64 * kBK * 2), &tmB, fb, n0 + 64 * j,

@@ -21,7 +21,9 @@
 //   - Tiles: static (pair c takes tiles c, c + pairs, ...) or dynamic: the
 //     leader's producer takes the next tile from a global counter and hands
 //     its index to every role of both CTAs through a 4-deep ring in shared
-//     memory. Dynamic keeps the tiles in flight a contiguous run of the
+//     memory. The last pair to run out of tiles resets the counter (and the
+//     count of finished pairs beside it), so no host-side reset is enqueued
+//     between launches. Dynamic keeps the tiles in flight a contiguous run of the
 //     raster order, so operand panels shared by neighbouring tiles are read
 //     from HBM about once instead of once per drifting pair.
 //   - Wide tiles (WIDE): 256 x 512 per pair, two N = 256 MMAs per k-step
@@ -269,7 +271,18 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             break;
           }
           t = atomicAdd(p.tile_counter, 1);
-          if (t >= num_pair_tiles) t = -1;
+          if (t >= num_pair_tiles) {
+            t = -1;
+            // this pair takes no more tiles: count it; the last pair of the
+            // launch sets both counters back to zero for the next launch (every
+            // pair's last take of a tile comes before its count)
+            __threadfence();
+            if (atomicAdd(p.tile_counter + 1, 1) == num_clusters - 1) {
+              __threadfence();
+              atomicExch(p.tile_counter, 0);
+              atomicExch(p.tile_counter + 1, 0);
+            }
+          }
           ring[slot] = t;
           st_shared_cluster_u32(mapa_shared(ring_s + 4u * slot, 1), (uint32_t)t);
           mbar_arrive_remote(mapa_shared(tile_full0 + 8u * slot, 0));
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
               const uint32_t dst = sB + stage * C::kStageBBytes + h * C::kBPartBytes;
               const int col = n_col + 256 * h;
               if (B_MN && p.b_mn_3d) {
-                tma_load_3d_pair(dst, &tmB, fb, 0, kb * kBK, col / 64);
+                tma_load3_pair(dst, &tmB, fb, 0, kb * kBK, col / 64, hb, pol_b);
               } else if (B_MN) {
                 tma_load_pair(dst, &tmB, fb, col, kb * kBK, hb, pol_b);
                 tma_load_pair(dst + 64 * kBK * 2, &tmB, fb, col + 64, kb * kBK, hb, pol_b);

@@ -34,24 +34,47 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kStatusBytes + 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+// the driver context each cached address belongs to: a device reset (or any
+// teardown and re-creation of the context) reloads the module, and the
+// address is then looked up again
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-gf_status fail(gf_status s) { return s; }
+// the status is also the thread's last error (gf_last_error)
+gf_status fail(gf_status s) { return gf::runtime_fail(s); }
 
-// Once per device, with that device current: the device address of the
-// scratch array.
+// Once per device and context, with that device current: the device address
+// of the scratch array.
 gf_status scratch_for_device(int dev, unsigned char** out) {
   if (dev < 0 || dev >= kMaxDevices) return GF_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
-    if (cudaSetDevice(dev) != cudaSuccess) return GF_ERR_CUDA;
+  if (cudaSetDevice(dev) != cudaSuccess) return GF_ERR_CUDA;
+  const CUcontext ctx = gf::runtime_current_context();
+  if (!g_scratch_addr[dev] || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
+      g_scratch_addr[dev] = nullptr;
       return GF_ERR_CUDA;
     }
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = gf::runtime_current_context();
   }
   *out = static_cast<unsigned char*>(g_scratch_addr[dev]);
+  return GF_OK;
+}
+
+// The calling thread's device, checked to be one the kernels run on.
+gf_status noalloc_device(int* dev, int* sms) {
+  gf_status st = gf::runtime_current_device(dev);
+  if (st != GF_OK) return st;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess) {
+    cudaGetLastError();
+    return GF_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return GF_ERR_UNSUPPORTED;
   return GF_OK;
 }
 
@@ -80,15 +103,9 @@ GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtyp
   }
   if (n > 0 && (!bgrad || !aligned16(bgrad))) return fail(GF_ERR_INVALID_VALUE);
 
-  int dev = 0;
-  gf_status st = gf::runtime_current_device(&dev);
+  int dev = 0, sms = 0;
+  gf_status st = noalloc_device(&dev, &sms);
   if (st != GF_OK) return fail(st);
-  int major = 0, minor = 0, sms = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return fail(GF_ERR_CUDA);
-  if (major != 10 || minor != 3) return fail(GF_ERR_UNSUPPORTED);
   unsigned char* scratch = nullptr;
   st = scratch_for_device(dev, &scratch);
   if (st != GF_OK) return fail(st);
@@ -157,6 +174,32 @@ GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtyp
   if (gf::launch_bgrad_finalize(partials, static_cast<int>(m_blocks), static_cast<int>(n), bgrad,
                                 s, 1) != cudaSuccess)
     return fail(GF_ERR_CUDA);
+  return GF_OK;
+}
+
+GF_API gf_status gf_noalloc_status(struct CUstream_st* stream) {
+  int dev = 0, sms = 0;
+  gf_status st = noalloc_device(&dev, &sms);
+  if (st != GF_OK) return fail(st);
+  unsigned char* scratch = nullptr;
+  st = scratch_for_device(dev, &scratch);
+  if (st != GF_OK) return fail(st);
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GF_ERR_CUDA);
+  }
+  int32_t word = 0;
+  if (cudaMemcpy(&word, scratch, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GF_ERR_CUDA);
+  }
+  if (word != 0) {
+    if (cudaMemset(scratch, 0, sizeof word) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(GF_ERR_CUDA);
+    }
+    return fail(GF_ERR_DEVICE_TIMEOUT);
+  }
   return GF_OK;
 }
 

@@ -75,7 +75,9 @@ struct GemmParams {
   int32_t drop_load;  // test hook: 1-based index of a stage load to skip (0: none)
   int32_t l2_hint_a;  // L2 policy of the A loads: 0 none, 1 evict first, 2 evict last
   int32_t l2_hint_b;  // ... of the B loads
-  int* tile_counter;  // CTA-pair kernel: global tile counter of the dynamic schedule (null: static)
+  // CTA-pair kernel, dynamic schedule (null: static): [0] the next tile to
+  // take, [1] pairs that have run out of tiles; both zero between launches
+  int* tile_counter;
   int32_t b_mn_3d;    // MN-major B through a 3-D map: one box per k-slice brings every
                       // 64-column chunk of the tile (0: one 2-D box per chunk)
   // single-CTA kernel, split k: each tile's k-blocks are shared by k_splits

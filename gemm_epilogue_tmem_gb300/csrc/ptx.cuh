@@ -425,6 +425,46 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t x, int32_t y, int32_t z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t cluster_bar, int32_t x, int32_t y,
+                                                      int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y), "r"(z),
+      "l"(policy)
+      : "memory");
+}
+
+// 3-D loads, hinted when the plan asks for an L2 policy
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int32_t x, int32_t y, int32_t z, int hint,
+                                          uint64_t policy) {
+  if (hint)
+    tma_load_3d_hint(dst, map, bar, x, y, z, policy);
+  else
+    tma_load_3d(dst, map, bar, x, y, z);
+}
+
+__device__ __forceinline__ void tma_load3_pair(uint32_t dst, const CUtensorMap* map,
+                                               uint32_t cluster_bar, int32_t x, int32_t y,
+                                               int32_t z, int hint, uint64_t policy) {
+  if (hint)
+    tma_load_3d_pair_hint(dst, map, cluster_bar, x, y, z, policy);
+  else
+    tma_load_3d_pair(dst, map, cluster_bar, x, y, z);
+}
+
 __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map,
                                               uint32_t cluster_bar, int32_t x, int32_t y,
                                               int hint, uint64_t policy) {

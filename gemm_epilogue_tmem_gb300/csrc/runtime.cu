@@ -16,6 +16,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "gf.h"
 #include "launch.h"
@@ -58,6 +59,19 @@ struct gf_plan {
   size_t splitk_bytes;   // capacity of d_splitk
   size_t splitk_cnt_offset;
   int pdl;               // 1: launches overlap their set-up with the previous kernel
+  // Tensor maps of the last execute, reused while the operand pointers and
+  // the plan's tiling are unchanged (encoding them is host work on every
+  // call otherwise). `gen` counts tiling changes; the cache is valid for
+  // cache_gen == gen.
+  uint64_t gen;
+  uint64_t cache_gen;
+  bool cache_valid;
+  const void* cache_A;
+  const void* cache_B;
+  const void* cache_B2;
+  bool cache_b_mn_3d;
+  CUtensorMap cache_tmA, cache_tmB, cache_tmB2;
+  std::mutex cache_mu;
 };
 
 namespace {
@@ -76,6 +90,7 @@ constexpr size_t kMaxSplitkBytes = size_t(256) << 20;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 PFN_cuCtxGetDevice_v2000 g_ctx_get_device = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
 std::once_flag g_driver_once;
 
 void load_driver_entry_points() {
@@ -91,6 +106,11 @@ void load_driver_entry_points() {
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       g_ctx_get_device = reinterpret_cast<PFN_cuCtxGetDevice_v2000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
   });
 }
 
@@ -289,6 +309,7 @@ gf_status ensure_splitk(gf_plan* p) {
 
 // plan_tiles, then the workspace the new tiling needs
 gf_status replan(gf_plan* p) {
+  ++p->gen;  // the tensor maps' boxes may change with the tiling
   plan_tiles(p);
   return ensure_splitk(p);
 }
@@ -354,7 +375,7 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
     return nullptr;
   }
 
-  gf_plan* p = static_cast<gf_plan*>(calloc(1, sizeof(gf_plan)));
+  gf_plan* p = new (std::nothrow) gf_plan();
   if (!p) {
     fail(GF_ERR_OUT_OF_MEMORY);
     return nullptr;
@@ -391,13 +412,13 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
 
   if (cudaMalloc(&p->d_status, 256) != cudaSuccess) {
     cudaGetLastError();
-    free(p);
+    delete p;
     fail(GF_ERR_OUT_OF_MEMORY);
     return nullptr;
   }
   if (cudaMemset(p->d_status, 0, 256) != cudaSuccess) {
     cudaFree(p->d_status);
-    free(p);
+    delete p;
     fail(GF_ERR_CUDA);
     return nullptr;
   }
@@ -407,7 +428,7 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
     if (cudaMalloc(&p->d_partials, p->partial_bytes) != cudaSuccess) {
       cudaGetLastError();
       cudaFree(p->d_status);
-      free(p);
+      delete p;
       fail(GF_ERR_OUT_OF_MEMORY);
       return nullptr;
     }
@@ -415,7 +436,7 @@ gf_plan* plan_create(int64_t m, int64_t n, int64_t k, gf_dtype dtype, int epi,
   if (ensure_splitk(p) != GF_OK) {
     if (p->d_partials) cudaFree(p->d_partials);
     cudaFree(p->d_status);
-    free(p);
+    delete p;
     fail(GF_ERR_OUT_OF_MEMORY);
     return nullptr;
   }
@@ -474,14 +495,23 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   memset(&tmA, 0, sizeof tmA);
   memset(&tmB, 0, sizeof tmB);
   memset(&tmB2, 0, sizeof tmB2);
-  if (p->k > 0) {
+  gf_plan* pm = const_cast<gf_plan*>(p);  // the map cache only
+  std::unique_lock<std::mutex> cache_lock(pm->cache_mu);
+  const bool cached = p->k > 0 && p->cache_valid && p->cache_gen == p->gen && p->cache_A == x.A &&
+                      p->cache_B == x.B && (!dual || p->cache_B2 == x.B2);
+  if (cached) {
+    tmA = p->cache_tmA;
+    tmB = p->cache_tmB;
+    tmB2 = p->cache_tmB2;
+    b_mn_3d = p->cache_b_mn_3d;
+  } else if (p->k > 0) {
     if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
     // K-major B boxes: a pair CTA loads half of the tile's columns, or with
     // two B operands all of the tile's columns of one operand
     const uint32_t rows_nk = p->pair && !dual ? 128u : static_cast<uint32_t>(p->tile_n);
     // MN-major B: one 3-D box per k-slice for all of this CTA's column
     // chunks when n is a multiple of 64, else one 2-D box per chunk
-    b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 && p->l2_hint_b == 0 &&
+    b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 &&
               encode_mn_3d(&tmB, x.B, p->dtype, p->n, p->k, 64, rows_nk / 64);
     const bool ok = b_mn_3d ||
                     (p->b_layout == GF_B_KN
@@ -490,7 +520,17 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
     if (!ok) return fail(GF_ERR_INVALID_VALUE);
     if (dual && !encode_2d(&tmB2, x.B2, p->dtype, p->k, p->n, 64, rows_nk))
       return fail(GF_ERR_INVALID_VALUE);
+    pm->cache_tmA = tmA;
+    pm->cache_tmB = tmB;
+    pm->cache_tmB2 = tmB2;
+    pm->cache_b_mn_3d = b_mn_3d;
+    pm->cache_A = x.A;
+    pm->cache_B = x.B;
+    pm->cache_B2 = dual ? x.B2 : nullptr;
+    pm->cache_gen = p->gen;
+    pm->cache_valid = true;
   }
+  cache_lock.unlock();
 
   gf::GemmParams prm;
   memset(&prm, 0, sizeof prm);
@@ -524,10 +564,10 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
         reinterpret_cast<int32_t*>(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset);
   }
   if (p->pair && !p->static_schedule && !p->one_tile_per_cta) {
-    // the tile counter sits in the plan's status block, 64 bytes past the status word
+    // the tile counter and the count of pairs that have finished sit in the
+    // plan's status block, 64 bytes past the status word; both are zero
+    // between launches (the last pair of a launch resets them)
     prm.tile_counter = p->d_status + 16;
-    if (cudaMemsetAsync(prm.tile_counter, 0, sizeof(int), st) != cudaSuccess)
-      return fail(GF_ERR_CUDA);
   }
 
   const bool atomic = has_bgrad(e) && p->bgrad_mode == GF_BGRAD_ATOMIC;
@@ -582,6 +622,15 @@ namespace gf {
 
 // Shared with the other host entry points of the library (runtime_internal.h).
 gf_status runtime_current_device(int* dev) { return current_device(dev); }
+
+CUcontext runtime_current_context() {
+  load_driver_entry_points();
+  CUcontext c = nullptr;
+  if (!g_ctx_get_current || g_ctx_get_current(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+gf_status runtime_fail(gf_status s) { return fail(s); }
 
 bool runtime_encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner,
                        uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
@@ -663,6 +712,7 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
         return fail(GF_ERR_INVALID_VALUE);
       p->l2_hint_a = static_cast<int>(value / 10);
       p->l2_hint_b = static_cast<int>(value % 10);
+      ++p->gen;  // the B map's form depends on the hint
       return GF_OK;
     case GF_OPT_SCHEDULE:
       if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
@@ -822,7 +872,9 @@ GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {
     // which waits gave up: 1 producer, 2 MMA on a stage, 4 MMA on an
     // accumulator buffer, 8 epilogue, 16 teardown drain
     if (getenv("GF_DEBUG")) fprintf(stderr, "gf: device status word 0x%x\n", word);
-    if (cudaMemset(p->d_status, 0, 4) != cudaSuccess) return fail(GF_ERR_CUDA);
+    // the status word, and the dynamic schedule's tile counters that a launch
+    // which gave up may leave part-way
+    if (cudaMemset(p->d_status, 0, 256) != cudaSuccess) return fail(GF_ERR_CUDA);
     // a launch that gave up may leave split-k counters part-way
     if (p->k_splits > 1 &&
         cudaMemset(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset, 0,
@@ -839,7 +891,7 @@ GF_API void gf_plan_free(gf_plan* p) {
   if (p->d_partials) cudaFree(p->d_partials);
   if (p->d_splitk) cudaFree(p->d_splitk);
   if (p->d_status) cudaFree(p->d_status);
-  free(p);
+  delete p;
 }
 
 }  // extern "C"

@@ -343,13 +343,16 @@ GF_API gf_status gf_plan_k_splits(const gf_plan* plan, int32_t* k_splits);
  * process exits. ceil(m/128) * n must not exceed GF_NOALLOC_MAX_PARTIALS
  * (else GF_ERR_UNSUPPORTED, nothing enqueued).
  *
- * The first call on a device looks up the array's device address for that
- * device (cudaGetSymbolAddress; no allocation); make that first call before
- * any stream capture. Every call shares the one array and reuses it as the
- * previous call left it: calls that overlap on the GPU (other streams, other
- * threads) race on it and must be serialised by the caller. A bounded wait
- * that gives up inside the kernel is recorded in the array's status word but
- * is not reported by this call.
+ * The first call on a device (and the first after its context was torn down
+ * and re-created, e.g. by a device reset) looks up the array's device
+ * address for that device (cudaGetSymbolAddress; no allocation); make that
+ * first call before any stream capture. Every call shares the one array and
+ * reuses it as the previous call left it: each call clears the status word on
+ * its stream before its kernel starts, and every partial sum the finalize
+ * reads is written by that call's kernel; calls that overlap on the GPU
+ * (other streams, other threads) race on it and must be serialised by the
+ * caller. A bounded wait that gives up inside the kernel is recorded in the
+ * array's status word; gf_noalloc_status reports it.
  *
  * Returns GF_OK, GF_ERR_INVALID_VALUE (bad size, enum, NULL or misaligned
  * pointer), GF_ERR_UNSUPPORTED (n or k not a multiple of 8, beyond the
@@ -361,6 +364,18 @@ GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtyp
                                         gf_b_layout b_layout, const void* A, const void* B,
                                         void* out, const void* aux_in, float* bgrad,
                                         struct CUstream_st* stream);
+
+/*
+ * The status of gf_drelu_bgrad_noalloc on the calling thread's current
+ * device, the counterpart of gf_plan_status for that allocation-free call
+ * (it allocates nothing either). Synchronises `stream`, then reads the
+ * status word of the library's fixed scratch array: GF_ERR_DEVICE_TIMEOUT
+ * (and the word is cleared) if a bounded wait in the most recent call's
+ * kernel gave up, whose outputs are then incomplete; GF_ERR_CUDA if the
+ * stream reports an error; else GF_OK. GF_ERR_NO_DEVICE / GF_ERR_UNSUPPORTED
+ * as gf_drelu_bgrad_noalloc. The pages have no counterpart.
+ */
+GF_API gf_status gf_noalloc_status(struct CUstream_st* stream);
 
 /* Release the plan and its workspace ("free" on the nvmath-python / cuBLASLt
  * page, step 3). Caller tensors are untouched. NULL is a no-op. Work already

@@ -85,3 +85,18 @@ def test_header_compiles_as_c(tmp_path):
     src.write_text('#include "gf.h"\nint main(void){ return (int)GF_OK + (int)sizeof(gf_status); }\n')
     rc = os.system(f"gcc -std=c99 -Wall -Werror -I{ROOT}/include -c {src} -o {tmp_path}/t.o")
     assert rc == 0
+
+
+def test_noalloc_rejection_is_the_last_error(L):
+    """A rejected gf_drelu_bgrad_noalloc is what gf_last_error reports (the
+    checks run before any device is touched)."""
+    assert L.gf_plan_set_option(None, 0, 0) == gf.GF_ERR_INVALID_VALUE
+    assert L.gf_last_error() == gf.GF_ERR_INVALID_VALUE
+    # n not a multiple of 8
+    assert L.gf_drelu_bgrad_noalloc(8, 12, 8, 0, 1, None, None, None, None, None, None) == \
+        gf.GF_ERR_UNSUPPORTED
+    assert L.gf_last_error() == gf.GF_ERR_UNSUPPORTED
+    # negative m
+    assert L.gf_drelu_bgrad_noalloc(-1, 8, 8, 0, 1, None, None, None, None, None, None) == \
+        gf.GF_ERR_INVALID_VALUE
+    assert L.gf_last_error() == gf.GF_ERR_INVALID_VALUE
