@@ -51,3 +51,25 @@ def test_recorded_traffic_matches_sources():
     # the committed profile is read back only while its digest matches the sources
     t = bench.recorded_traffic()
     assert t is None or (len(t) == 2 and all(v > 3e9 for v in t))
+
+
+def test_pick_peak_burst_and_sustained():
+    pk = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    assert bench.pick_peak(pk, "measured", 0.4)[0] == 1900.0   # short loop: burst
+    assert bench.pick_peak(pk, "measured", 4.0)[0] == 1700.0   # seconds-long loop: sustained
+    assert bench.pick_peak({"bf16_tflops": 1900.0}, "fallback", 9.0)[0] == 1900.0
+
+
+def test_stats_and_parity_block():
+    st = bench.stats_ms([3.0, 1.0, 2.0, 10.0])
+    assert st["median"] == 2.5 and st["min"] == 1.0 and st["n"] == 4
+    ok = bench._parity_block({"Y": {"nmax": 1e-3, "rel_l2": 1e-4},
+                              "bgrad": {"nmax": 5e-3, "rel_l2": 5e-3}}, bgrad_keys=("bgrad",))
+    assert ok["pass"]
+    # an output error above the output bound fails; the same error on a bias
+    # gradient key is held to the bias-gradient bound
+    bad = bench._parity_block({"Y": {"nmax": 1e-3, "rel_l2": 6e-3}})
+    assert not bad["pass"]
+    assert not bench._parity_block({"Y": {"nmax": 0.0, "rel_l2": 0.0}},
+                                   mask={"mask_mismatch_outside_band": 1,
+                                         "mask_mismatch_in_band": 0})["pass"]
