@@ -58,7 +58,7 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
   attr[1].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.params);
+  return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.tmOut, *a.tmAux, *a.params);
 }
 
 // Largest number of CTA pairs of this instance that can be resident at once.

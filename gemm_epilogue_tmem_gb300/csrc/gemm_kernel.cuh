@@ -188,6 +188,40 @@ __device__ __forceinline__ void store_rows32_staged(T* base, int M, int N, int r
   __syncwarp();
 }
 
+// The same 32 x 32 block written by one 2-D TMA store from the staging buffer
+// (its XOR permutation of 16-byte pieces by (row / 2) % 4 is the tensor map's
+// 64-byte swizzle, so the box's rows land where the map expects them; rows
+// and columns outside the tensor are not written). The store is issued by
+// lane 0 and tracked by its bulk groups; the buffer is written again only
+// after that store has read it. Nothing of it is left in flight for a later
+// release fence of the warp to wait for. Called by all 32 lanes.
+template <typename T>
+__device__ __forceinline__ void store_rows32_tma(const CUtensorMap* map, int row0w, int col0,
+                                                 const float* v, uint32_t lane, uint32_t stg) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack2<T>(v[2 * i], v[2 * i + 1]);
+  if (lane == 0) bulk_wait_read_all();  // the previous store from this buffer has read it
+  __syncwarp();
+  const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+  for (uint32_t pc = 0; pc < 4; ++pc)
+    st_shared_v4(stg + lane * 64u + ((pc ^ sw) << 4), w[4 * pc], w[4 * pc + 1], w[4 * pc + 2],
+                 w[4 * pc + 3]);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, stg, col0, row0w);
+    bulk_commit();
+  }
+}
+
+// relu_aux words of a drain over 4 chunks kept in registers, so that they are
+// stored after the accumulator release (TMA-store drains)
+struct AuxWords {
+  uint32_t w0, w1, w2, w3;
+};
+
 // this lane's 32 values of row `row` (direct) or the warp's 32 rows (staged)
 template <typename T, bool STG>
 __device__ __forceinline__ void emit_row32(T* base, int M, int N, int row0w, int col0,
@@ -321,11 +355,19 @@ __device__ __forceinline__ void side_ring_prefetch(const GemmParams& p, int row0
 // SRING > 0 (dSwiGLU with the staging buffer): the side inputs come from
 // this warp's ring of SRING chunk slots at `side`, whose first SRING chunks
 // side_ring_prefetch has issued; the drain keeps SRING chunks in flight.
+// TMA: the 16-bit outputs leave through the staging buffer by TMA stores
+// (tm_out for out, tm_aux for the 16-bit aux_out), and relu_aux words are
+// left in `words` for the caller to store after releasing the accumulator
+// (BN <= 128: at most 4 chunks).
 template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false,
-          int SRING = 0>
+          int SRING = 0, bool TMA = false>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red,
-                                               uint32_t stg = 0, uint32_t side = 0) {
+                                               uint32_t stg = 0, uint32_t side = 0,
+                                               const CUtensorMap* tm_out = nullptr,
+                                               const CUtensorMap* tm_aux = nullptr,
+                                               AuxWords* words = nullptr) {
+  static_assert(!TMA || (STG && BN <= 128), "TMA-store drains: staged, at most 4 chunks");
   constexpr bool kDual = epi_dual(EPI);
   // 16-byte side inputs per chunk: g and u (DSWIGLU), the pre-activation
   // (DGELU_BGRAD), the column bias (bias epilogs), the mask word (DRELU_BGRAD)
@@ -344,7 +386,6 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   if constexpr (epi_has_bias(EPI)) {
     if (p.bias_axis == 1 && row_ok) row_bias = to_f32<T>(bias[row]);
   }
-  T* out = reinterpret_cast<T*>(p.out);
   const bool has_acc = p.num_k_blocks > 0;
   const int nch = min(BN / 32, (p.N - n0 + 31) / 32);  // chunks with columns below N
   constexpr bool kRing = SRING > 0;
@@ -353,6 +394,16 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
     if constexpr (kRing) cp_async_wait_all();
     return;
   }
+
+  // one 32 x 32 block of a 16-bit output: `aux` selects aux_out over out
+  auto emit = [&](bool aux, int col0, const float* vals) {
+    if constexpr (TMA) {
+      store_rows32_tma<T>(aux ? tm_aux : tm_out, row0w, col0, vals, lane, stg);
+    } else {
+      emit_row32<T, STG>(reinterpret_cast<T*>(aux ? p.aux_out : p.out), p.M, p.N, row0w, col0,
+                         vals, lane, stg);
+    }
+  };
 
   // the saved 16-bit activations are read coalesced when the staging buffer
   // is there: lane l loads 16 bytes of row 8g + l/4 (4 lanes per 64-byte row
@@ -460,6 +511,10 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       cp_async_commit();
     } else if constexpr (kCoalesced) {
       // through the staging buffer: rows as loaded -> this lane's row
+      if constexpr (TMA) {
+        if (lane == 0) bulk_wait_read_all();  // a TMA store may still be reading it
+        __syncwarp();
+      }
 #pragma unroll
       for (int in = 0; in < (EPI == EPI_DSWIGLU ? 2 : 1); ++in) {
 #pragma unroll
@@ -514,7 +569,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
           v[8 * g + i] = dh * u8[i] * s * (1.f + g8[i] * (1.f - s));
         }
       }
-      emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, dup, lane, stg);
+      emit(true, col0, dup);
     } else if constexpr (EPI == EPI_DGELU_BGRAD) {
       // saved pre-activation z of this row's 32 columns
 #pragma unroll
@@ -552,8 +607,14 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
         for (int j = 0; j < 32; ++j) b4[j & 3] |= (v[j] > 0.f ? 1u : 0u) << j;
         const uint32_t bits = row_ok ? (b4[0] | b4[1]) | (b4[2] | b4[3]) : 0u;
         const uint32_t my_word = bit_transpose32(bits, lane);
-        if (wrow_ok && col0 + (int)lane < p.N)
+        if constexpr (TMA) {
+          if (c == 0) words->w0 = my_word;
+          else if (c == 1) words->w1 = my_word;
+          else if (c == 2) words->w2 = my_word;
+          else words->w3 = my_word;
+        } else if (wrow_ok && col0 + (int)lane < p.N) {
           p.aux_out[(size_t)wrow * p.N + col0 + lane] = my_word;
+        }
       }
       if constexpr (EPI == EPI_RELU_BIAS || EPI == EPI_RELU_AUX_BIAS) {
 #pragma unroll
@@ -561,7 +622,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
       if constexpr (EPI == EPI_GELU_AUX_BIAS) {
         // the pre-activation, rounded to T, for the backward
-        emit_row32<T, STG>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, v, lane, stg);
+        emit(true, col0, v);
       }
       if constexpr (EPI == EPI_GELU_BIAS || EPI == EPI_GELU_AUX_BIAS) {
 #pragma unroll
@@ -569,7 +630,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
     }
 
-    emit_row32<T, STG>(out, p.M, p.N, row0w, col0, v, lane, stg);
+    emit(false, col0, v);
 
     if constexpr (epi_has_bgrad(EPI)) {
       // transpose-reduce: after 5 halving steps (31 shuffles) lane l

@@ -137,6 +137,21 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// relu_aux words of one TMA-store drain (4 chunks of 32 columns from n0h)
+// for the 32 rows of the warp starting at row0w; words past M or N are not
+// stored. Called by all 32 lanes.
+__device__ __forceinline__ void store_aux_words(const GemmParams& p, int row0w, int n0h,
+                                                uint32_t lane, const AuxWords& aw) {
+  if (row0w >= p.M) return;
+  uint32_t* dst = p.aux_out + (size_t)(row0w >> 5) * p.N;
+  const uint32_t w[4] = {aw.w0, aw.w1, aw.w2, aw.w3};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int col = n0h + 32 * c + (int)lane;
+    if (col < p.N) dst[col] = w[c];
+  }
+}
+
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
 __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
                                           pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
@@ -144,7 +159,9 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
                                   1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+                            const __grid_constant__ CUtensorMap tmB2,
+                            const __grid_constant__ CUtensorMap tmOut,
+                            const __grid_constant__ CUtensorMap tmAux, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
   using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
                     pair_side_ring(EPI, WIDE)>;
@@ -210,6 +227,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (NB == 2) prefetch_tmap(&tmB2);
+    }
+    if constexpr (WIDE) {
+      prefetch_tmap(&tmOut);
+      if constexpr (EPI == EPI_GELU_AUX_BIAS || EPI == EPI_DSWIGLU) prefetch_tmap(&tmAux);
     }
   }
   if (warp == 1) {
@@ -554,13 +575,19 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
-        // half 0, release it (the next tile's first MMAs go there), half 1
+        // half 0, release it (the next tile's first MMAs go there), half 1.
+        // The 16-bit outputs leave by TMA stores, and the relu_aux words are
+        // stored after the release, so that the release (a cluster-scope
+        // release) has no global stores of the drain to wait for.
         const uint32_t stg = stg0 + 2048u * (uint32_t)(warp - 2);
-        epilogue_drain<EPI, T, 128, BN, true, kSide>(p, t_row + (uint32_t)c_sub, row0, n0 + c_sub,
-                                                     q, lane, red + c_sub, stg, side);
+        AuxWords aw;
+        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true>(
+            p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side, &tmOut,
+            &tmAux, &aw);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader);
+        if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
         // half 1 is complete a few k-slices after half 0
         bool ok1 = mbar_wait_bounded(tfull0 + 8u, use, abort_flag, p.wait_limit_ns);
         if constexpr (epi_has_bgrad(EPI)) ok1 = !named_bar_red_or(1, NT, !ok1);
@@ -570,12 +597,14 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           break;
         }
         tc_fence_after();
-        epilogue_drain<EPI, T, 128, BN, true, kSide>(p, t_row + 256u + (uint32_t)c_sub, row0,
-                                                     n0 + 256 + c_sub, q, lane,
-                                                     red + 256 + c_sub, stg, side + kSideHalf);
+        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true>(
+            p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane, red + 256 + c_sub,
+            stg, side + kSideHalf, &tmOut, &tmAux, &aw);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
+        if constexpr (EPI == EPI_RELU_AUX_BIAS)
+          store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
       } else if constexpr (C::kEpiWarps == 8) {
         // this warp's half of the tile's columns
         constexpr int H = BN / 2;
@@ -595,6 +624,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       if constexpr (epi_has_bgrad(EPI)) epilogue_bgrad<BN, NT>(p, red, ep_tid, n0, row0 / kBM);
     }
     if constexpr (kRing > 0) cp_async_wait_all();  // no copy lands after the CTA is gone
+    if constexpr (WIDE) {
+      if (lane == 0) bulk_wait_all();  // this warp's TMA stores have completed
+      __syncwarp();
+    }
   }
 
   // a CTA that gave up may still have loads in flight towards its shared

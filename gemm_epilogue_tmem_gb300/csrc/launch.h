@@ -13,6 +13,10 @@ struct LaunchArgs {
   const CUtensorMap* tmA;
   const CUtensorMap* tmB;
   const CUtensorMap* tmB2;  // second B operand (SwiGLU up projection); else = tmB
+  // CTA-pair kernel with 256 x 512 tiles: the 16-bit outputs out and aux_out
+  // as TMA store targets (32 x 32 boxes, 64-byte swizzle); else = tmA
+  const CUtensorMap* tmOut;
+  const CUtensorMap* tmAux;
   const GemmParams* params;
   int grid;
   int bf16;     // 0: fp16, 1: bf16

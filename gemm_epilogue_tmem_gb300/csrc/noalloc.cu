@@ -161,6 +161,8 @@ GF_API gf_status gf_drelu_bgrad_noalloc(int64_t m, int64_t n, int64_t k, gf_dtyp
   la.tmA = &tmA;
   la.tmB = &tmB;
   la.tmB2 = &tmB;
+  la.tmOut = &tmA;  // the single-CTA kernel stores without tensor maps
+  la.tmAux = &tmA;
   la.params = &prm;
   la.grid = static_cast<int>(tiles < sms ? tiles : sms);
   la.bf16 = dtype == GF_BF16 ? 1 : 0;

@@ -474,6 +474,36 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
     tma_load_2d_pair(dst, map, cluster_bar, x, y);
 }
 
+// ----------------------------------------------------------- TMA stores
+// 2-D tiled store of one box from shared memory to global memory (elements
+// outside the tensor are not written), tracked by this thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// wait until this thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// wait until this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// make this thread's shared-memory writes visible to the tensor (async) proxy
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // named barrier over `count` threads (id 0 is __syncthreads)
 // Programmatic dependent launch. grid_dep_wait: wait until the grids this
 // launch depends on have completed and their memory operations are visible

@@ -69,8 +69,10 @@ struct gf_plan {
   const void* cache_A;
   const void* cache_B;
   const void* cache_B2;
+  const void* cache_out;
+  const void* cache_aux;
   bool cache_b_mn_3d;
-  CUtensorMap cache_tmA, cache_tmB, cache_tmB2;
+  CUtensorMap cache_tmA, cache_tmB, cache_tmB2, cache_tmOut, cache_tmAux;
   std::mutex cache_mu;
 };
 
@@ -164,6 +166,23 @@ bool encode_mn_3d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t n, ui
 
 // 2-D tensor map over a row-major [outer, inner] matrix of 16-bit elements,
 // boxes of box_inner x box_outer, 128-byte swizzle, zero fill out of bounds.
+// Store target of the 256 x 512 tiles' epilogue: a row-major [rows, cols]
+// matrix of 16-bit elements written in 32 x 32 boxes (64-byte rows) from a
+// staging buffer laid out with the 64-byte swizzle.
+bool encode_store_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t cols,
+                     uint64_t rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt == GF_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool encode_2d(CUtensorMap* map, const void* ptr, gf_dtype dt, uint64_t inner, uint64_t outer,
                uint32_t box_inner, uint32_t box_outer) {
   cuuint64_t dims[2] = {inner, outer};
@@ -490,43 +509,63 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
     return GF_OK;
   }
 
-  CUtensorMap tmA, tmB, tmB2;
+  CUtensorMap tmA, tmB, tmB2, tmOut, tmAux;
   bool b_mn_3d = false;
   memset(&tmA, 0, sizeof tmA);
   memset(&tmB, 0, sizeof tmB);
   memset(&tmB2, 0, sizeof tmB2);
+  memset(&tmOut, 0, sizeof tmOut);
+  memset(&tmAux, 0, sizeof tmAux);
+  // the 256 x 512 tiles store their 16-bit outputs by TMA
+  const bool store_maps = p->pair && p->wide;
+  const bool aux16 = e == gf::EPI_GELU_AUX_BIAS || e == gf::EPI_DSWIGLU;
   gf_plan* pm = const_cast<gf_plan*>(p);  // the map cache only
   std::unique_lock<std::mutex> cache_lock(pm->cache_mu);
-  const bool cached = p->k > 0 && p->cache_valid && p->cache_gen == p->gen && p->cache_A == x.A &&
-                      p->cache_B == x.B && (!dual || p->cache_B2 == x.B2);
+  const bool cached = p->cache_valid && p->cache_gen == p->gen && p->cache_A == x.A &&
+                      p->cache_B == x.B && (!dual || p->cache_B2 == x.B2) &&
+                      (!store_maps ||
+                       (p->cache_out == x.out && (!aux16 || p->cache_aux == x.aux_out)));
   if (cached) {
     tmA = p->cache_tmA;
     tmB = p->cache_tmB;
     tmB2 = p->cache_tmB2;
+    tmOut = p->cache_tmOut;
+    tmAux = p->cache_tmAux;
     b_mn_3d = p->cache_b_mn_3d;
-  } else if (p->k > 0) {
-    if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
-    // K-major B boxes: a pair CTA loads half of the tile's columns, or with
-    // two B operands all of the tile's columns of one operand
-    const uint32_t rows_nk = p->pair && !dual ? 128u : static_cast<uint32_t>(p->tile_n);
-    // MN-major B: one 3-D box per k-slice for all of this CTA's column
-    // chunks when n is a multiple of 64, else one 2-D box per chunk
-    b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 &&
-              encode_mn_3d(&tmB, x.B, p->dtype, p->n, p->k, 64, rows_nk / 64);
-    const bool ok = b_mn_3d ||
-                    (p->b_layout == GF_B_KN
-                         ? encode_2d(&tmB, x.B, p->dtype, p->n, p->k, 64, 64)
-                         : encode_2d(&tmB, x.B, p->dtype, p->k, p->n, 64, rows_nk));
-    if (!ok) return fail(GF_ERR_INVALID_VALUE);
-    if (dual && !encode_2d(&tmB2, x.B2, p->dtype, p->k, p->n, 64, rows_nk))
-      return fail(GF_ERR_INVALID_VALUE);
+  } else {
+    if (p->k > 0) {
+      if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
+      // K-major B boxes: a pair CTA loads half of the tile's columns, or with
+      // two B operands all of the tile's columns of one operand
+      const uint32_t rows_nk = p->pair && !dual ? 128u : static_cast<uint32_t>(p->tile_n);
+      // MN-major B: one 3-D box per k-slice for all of this CTA's column
+      // chunks when n is a multiple of 64, else one 2-D box per chunk
+      b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 &&
+                encode_mn_3d(&tmB, x.B, p->dtype, p->n, p->k, 64, rows_nk / 64);
+      const bool ok = b_mn_3d ||
+                      (p->b_layout == GF_B_KN
+                           ? encode_2d(&tmB, x.B, p->dtype, p->n, p->k, 64, 64)
+                           : encode_2d(&tmB, x.B, p->dtype, p->k, p->n, 64, rows_nk));
+      if (!ok) return fail(GF_ERR_INVALID_VALUE);
+      if (dual && !encode_2d(&tmB2, x.B2, p->dtype, p->k, p->n, 64, rows_nk))
+        return fail(GF_ERR_INVALID_VALUE);
+    }
+    if (store_maps) {
+      if (!encode_store_2d(&tmOut, x.out, p->dtype, p->n, p->m)) return fail(GF_ERR_INVALID_VALUE);
+      if (aux16 && !encode_store_2d(&tmAux, x.aux_out, p->dtype, p->n, p->m))
+        return fail(GF_ERR_INVALID_VALUE);
+    }
     pm->cache_tmA = tmA;
     pm->cache_tmB = tmB;
     pm->cache_tmB2 = tmB2;
+    pm->cache_tmOut = tmOut;
+    pm->cache_tmAux = tmAux;
     pm->cache_b_mn_3d = b_mn_3d;
     pm->cache_A = x.A;
     pm->cache_B = x.B;
     pm->cache_B2 = dual ? x.B2 : nullptr;
+    pm->cache_out = x.out;
+    pm->cache_aux = x.aux_out;
     pm->cache_gen = p->gen;
     pm->cache_valid = true;
   }
@@ -582,6 +621,8 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   la.tmA = &tmA;
   la.tmB = &tmB;
   la.tmB2 = dual ? &tmB2 : &tmB;
+  la.tmOut = &tmOut;
+  la.tmAux = &tmAux;
   la.params = &prm;
   la.grid = p->grid;
   la.bf16 = p->dtype == GF_BF16 ? 1 : 0;
