@@ -42,6 +42,15 @@ cudaError_t launch_pair_instance(const LaunchArgs& a) {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if constexpr (WIDE) {
+      // the wide kernel hands registers from its control warpgroup to its
+      // epilogue warpgroups (setmaxnreg); the split adds up only for this
+      // launch register count, so refuse to launch a build that differs
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kernel);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != C::kLaunchRegs) return cudaErrorInvalidKernelImage;
+    }
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};

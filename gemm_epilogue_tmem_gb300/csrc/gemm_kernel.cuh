@@ -359,15 +359,29 @@ __device__ __forceinline__ void side_ring_prefetch(const GemmParams& p, int row0
 // (tm_out for out, tm_aux for the 16-bit aux_out), and relu_aux words are
 // left in `words` for the caller to store after releasing the accumulator
 // (BN <= 128: at most 4 chunks).
+// PRELOAD (with TMA, one B operand, no side ring, 4 chunks): every chunk of
+// the accumulator is loaded from tensor memory first (128 fp32 registers per
+// thread: the caller runs with a raised register allowance), then `release`
+// is called -- the accumulator may be overwritten from then on -- and the
+// chunks are processed from registers. The MMAs that wait for this
+// accumulator then wait only for its tensor-memory reads, not for the
+// epilogue's arithmetic and stores.
+struct NoRelease {
+  __device__ __forceinline__ void operator()() const {}
+};
+
 template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false,
-          int SRING = 0, bool TMA = false>
+          int SRING = 0, bool TMA = false, bool PRELOAD = false, typename Release = NoRelease>
 __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red,
                                                uint32_t stg = 0, uint32_t side = 0,
                                                const CUtensorMap* tm_out = nullptr,
                                                const CUtensorMap* tm_aux = nullptr,
-                                               AuxWords* words = nullptr) {
+                                               AuxWords* words = nullptr,
+                                               Release release = Release()) {
   static_assert(!TMA || (STG && BN <= 128), "TMA-store drains: staged, at most 4 chunks");
+  static_assert(!PRELOAD || (TMA && !epi_dual(EPI) && SRING == 0 && BN == 128),
+                "preloaded drains: TMA stores, one operand, 4 chunks");
   constexpr bool kDual = epi_dual(EPI);
   // 16-byte side inputs per chunk: g and u (DSWIGLU), the pre-activation
   // (DGELU_BGRAD), the column bias (bias epilogs), the mask word (DRELU_BGRAD)
@@ -392,6 +406,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   static_assert(!kRing || (STG && EPI == EPI_DSWIGLU), "side ring: dSwiGLU with staging");
   if (nch <= 0) {
     if constexpr (kRing) cp_async_wait_all();
+    if constexpr (PRELOAD) release();
     return;
   }
 
@@ -462,55 +477,9 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
     }
   };
 
-  uint32_t ra[32];
-  uint32_t rb[kDual ? 32 : 1];
-  uint4 sd[kSideN];
-  if (has_acc) {
-    tmem_ld_32x32b_x32(t_row, ra);
-    if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN, rb);
-  }
-  if constexpr (!kRing) load_side(n0, sd);
-
-#pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
-    const int col0 = n0 + 32 * c;
-    float v[32];
-    float u2[kDual ? 32 : 1];  // the second accumulator (the SwiGLU "up" product)
-    if (has_acc) {
-      tmem_ld_wait_tied(ra);
-      if constexpr (kDual) tmem_tie(rb);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
-      if constexpr (kDual) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) u2[j] = __uint_as_float(rb[j]);
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      if constexpr (kDual) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) u2[j] = 0.f;
-      }
-    }
-    uint4 cur[kSideN];
-    if constexpr (kRing) {
-      // this chunk's slot is complete once at most SRING - 1 groups are pending
-      cp_async_wait_group<SRING - 1>();
-      __syncwarp();
-      const uint32_t slot = side + kSideSlotBytes * (uint32_t)(c % SRING);
-      const uint32_t sw = (lane >> 1) & 3u;
-#pragma unroll
-      for (int in = 0; in < 2; ++in) {
-#pragma unroll
-        for (uint32_t pc = 0; pc < 4; ++pc)
-          cur[4 * in + pc] = ld_shared_v4(slot + 2048u * in + lane * 64u + ((pc ^ sw) << 4));
-      }
-      __syncwarp();  // every lane has read the slot: refill it
-      if (c + SRING < nch) side_ring_issue<T>(p, row0w, col0 + 32 * SRING, lane, slot);
-      cp_async_commit();
-    } else if constexpr (kCoalesced) {
-      // through the staging buffer: rows as loaded -> this lane's row
+  // saved activations of the staging path: rows as loaded -> this lane's row
+  auto side_to_rows = [&](const uint4 (&sd)[kSideN], uint4 (&cur)[kSideN]) {
+    if constexpr (kCoalesced) {
       if constexpr (TMA) {
         if (lane == 0) bulk_wait_read_all();  // a TMA store may still be reading it
         __syncwarp();
@@ -535,14 +504,13 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
 #pragma unroll
       for (int i = 0; i < kSideN; ++i) cur[i] = sd[i];
     }
-    if (c + 1 < nch) {  // next chunk's loads, in flight while this one is processed
-      if (has_acc) {
-        tmem_ld_32x32b_x32(t_row + 32u * (c + 1), ra);
-        if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * (c + 1), rb);
-      }
-      if constexpr (!kRing) load_side(col0 + 32, sd);
-    }
+  };
 
+  // the epilog of chunk c (columns col0 = n0 + 32 c ..): v = the accumulator
+  // (u2 = the second one of the dual epilogs), cur = its side inputs
+  auto finish_chunk = [&](int c, float (&v)[32], float (&u2)[kDual ? 32 : 1],
+                          const uint4 (&cur)[kSideN]) {
+    const int col0 = n0 + 32 * c;
     if constexpr (kDual) {
       // gate+up SwiGLU: v = g = x Wg^T, u2 = u = x Wu^T; h = silu(g) * u
       if constexpr (EPI == EPI_SWIGLU_SAVE) {
@@ -647,6 +615,100 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
       }
       red[q * RS + 32 * c + (int)lane] = v[0];
     }
+  };
+
+  uint4 sd[kSideN];
+  if constexpr (PRELOAD) {
+    // every chunk out of tensor memory (BN registers per thread), then the
+    // accumulator is free again
+    uint32_t pre[BN / 32][32];
+    float u2[1];
+    if (has_acc) {
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld_32x32b_x32(t_row + 32u * c, pre[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_tie(pre[c]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pre[c][j] = 0u;  // nothing multiplied: zero
+    }
+    release();
+    load_side(n0, sd);
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      if (c < nch) {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(pre[c][j]);
+        uint4 cur[kSideN];
+        side_to_rows(sd, cur);
+        if (c + 1 < nch) load_side(n0 + 32 * (c + 1), sd);
+        finish_chunk(c, v, u2, cur);
+      }
+    }
+    return;
+  }
+
+  uint32_t ra[32];
+  uint32_t rb[kDual ? 32 : 1];
+  if (has_acc) {
+    tmem_ld_32x32b_x32(t_row, ra);
+    if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN, rb);
+  }
+  if constexpr (!kRing) load_side(n0, sd);
+
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const int col0 = n0 + 32 * c;
+    float v[32];
+    float u2[kDual ? 32 : 1];  // the second accumulator (the SwiGLU "up" product)
+    if (has_acc) {
+      tmem_ld_wait_tied(ra);
+      if constexpr (kDual) tmem_tie(rb);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(ra[j]);
+      if constexpr (kDual) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u2[j] = __uint_as_float(rb[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      if constexpr (kDual) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u2[j] = 0.f;
+      }
+    }
+    uint4 cur[kSideN];
+    if constexpr (kRing) {
+      // this chunk's slot is complete once at most SRING - 1 groups are pending
+      cp_async_wait_group<SRING - 1>();
+      __syncwarp();
+      const uint32_t slot = side + kSideSlotBytes * (uint32_t)(c % SRING);
+      const uint32_t sw = (lane >> 1) & 3u;
+#pragma unroll
+      for (int in = 0; in < 2; ++in) {
+#pragma unroll
+        for (uint32_t pc = 0; pc < 4; ++pc)
+          cur[4 * in + pc] = ld_shared_v4(slot + 2048u * in + lane * 64u + ((pc ^ sw) << 4));
+      }
+      __syncwarp();  // every lane has read the slot: refill it
+      if (c + SRING < nch) side_ring_issue<T>(p, row0w, col0 + 32 * SRING, lane, slot);
+      cp_async_commit();
+    } else {
+      side_to_rows(sd, cur);
+    }
+    if (c + 1 < nch) {  // next chunk's loads, in flight while this one is processed
+      if (has_acc) {
+        tmem_ld_32x32b_x32(t_row + 32u * (c + 1), ra);
+        if constexpr (kDual) tmem_ld_32x32b_x32(t_row + (uint32_t)BN + 32u * (c + 1), rb);
+      }
+      if constexpr (!kRing) load_side(col0 + 32, sd);
+    }
+    finish_chunk(c, v, u2, cur);
   }
 }
 

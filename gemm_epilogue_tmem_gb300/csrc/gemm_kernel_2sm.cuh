@@ -89,7 +89,22 @@ struct PairCfg {
   // epilogue warps: EPI8 drains with two warps per TMEM lane quarter (each
   // takes half of the columns)
   static constexpr int kEpiWarps = EPI8 ? 8 : 4;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  // warps before the epilogue warps: producer, MMA; wide: + two idle warps,
+  // so that the control and the epilogue roles are whole warpgroups whose
+  // registers can be redistributed (setmaxnreg): the epilogue warps of the
+  // wide tiles hold a quarter's worth of the accumulator in registers
+  static constexpr int kCtlWarps = WIDE ? 4 : 2;
+  static constexpr int kThreads = 32 * (kCtlWarps + kEpiWarps);
+  // wide: registers per thread at launch (65536 / 384, in steps of 8), and
+  // after the redistribution: control warpgroup 56, epilogue warpgroups 224
+  static constexpr int kLaunchRegs = WIDE ? 168 : 0;
+  static constexpr int kCtlRegs = 56;
+  static constexpr int kEpiRegs = 224;
+  static_assert(!WIDE || (kCtlWarps == 4 && kEpiWarps == 8 &&
+                          32 * (kCtlWarps * kCtlRegs + kEpiWarps * kEpiRegs) <=
+                              kThreads * kLaunchRegs &&
+                          kThreads * kLaunchRegs <= 65536),
+                "register redistribution within the launch's registers");
   // consumers of a tile index: leader MMA + peer producer + both CTAs' epilogue warps
   static constexpr int kTileConsumers = 2 + 2 * kEpiWarps;
   static constexpr int kCtrlBytes = kSmemCtrlBytes;
@@ -199,7 +214,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   const int warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   // dSwiGLU: an epilogue warp's side-input ring (kRing slots) after the staging buffers
-  const uint32_t sring = side0 + kRing * kSideSlotBytes * (uint32_t)(warp >= 2 ? warp - 2 : 0);
+  const int ew = warp - C::kCtlWarps;  // epilogue warp index (negative: other roles)
+  const uint32_t sring = side0 + kRing * kSideSlotBytes * (uint32_t)(ew >= 0 ? ew : 0);
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int cluster_id = blockIdx.x >> 1;
@@ -266,6 +282,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
     return t;
   };
 
+  if (warp < C::kCtlWarps) {
+    // control warps: warpgroup 0 of the wide tiles gives registers to the
+    // two epilogue warpgroups (the host checks the launch's register count)
+    if constexpr (WIDE) setmaxnreg_dec<C::kCtlRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && (p.num_k_blocks > 0 || dynamic)) {
@@ -521,14 +541,16 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         raise_error(p, abort_flag, ST_TIMEOUT_DRAIN);
     }
     __syncwarp();
+  }  // warps 2 and 3 of the wide tiles' control warpgroup have no role
   } else {
+    if constexpr (WIDE) setmaxnreg_inc<C::kEpiRegs>();
     // ------------------------------------------------------------ epilogue
     // warp w drains TMEM lanes 32 (w % 4)..; with 8 epilogue warps (wide) the
     // two warps of a lane quarter take column halves `sub` 0 and 1
     constexpr int NT = 32 * C::kEpiWarps;  // epilogue threads
     const int q = warp & 3;
-    const int sub = (warp - 2) >> 2;
-    const int ep_tid = threadIdx.x - 64;
+    const int sub = ew >> 2;
+    const int ep_tid = threadIdx.x - 32 * C::kCtlWarps;
     const uint32_t tempty_leader = mapa_shared(tempty0, 0);
     for (int it = 0;; ++it) {
       // every lane reads the index; lane 0 releases the slot for the warp
@@ -554,7 +576,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       constexpr bool kSide = WIDE && (EPI == EPI_DRELU_BGRAD || epi_has_bias(EPI));
       constexpr uint32_t kSideHalf = EPI == EPI_DRELU_BGRAD ? 512u : 256u;  // 128 columns
       const int c_sub = 128 * sub;
-      const uint32_t side = side0 + 1024u * (uint32_t)(warp - 2);
+      const uint32_t side = side0 + 1024u * (uint32_t)ew;
       if constexpr (kSide) {
         prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + c_sub, lane, side);
         prefetch_side<EPI, T, 128>(p, row0 + 32 * q, n0 + 256 + c_sub, lane, side + kSideHalf);
@@ -575,18 +597,24 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
-        // half 0, release it (the next tile's first MMAs go there), half 1.
-        // The 16-bit outputs leave by TMA stores, and the relu_aux words are
-        // stored after the release, so that the release (a cluster-scope
-        // release) has no global stores of the drain to wait for.
-        const uint32_t stg = stg0 + 2048u * (uint32_t)(warp - 2);
+        // half 0, then half 1: each warp loads its 128 columns of the half
+        // out of tensor memory and releases the half at once (the next
+        // tile's first MMAs go to half 0), then applies the epilog from
+        // registers. The 16-bit outputs leave by TMA stores and the relu_aux
+        // words are stored after the release, so that the release (a
+        // cluster-scope release) has no global stores to wait for.
+        const uint32_t stg = stg0 + 2048u * (uint32_t)ew;
         AuxWords aw;
-        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true>(
+        // (a relaxed arrive: the accumulator's reads have completed before
+        // it, and it must not wait for this warp's TMA stores in flight)
+        auto release_half = [&](uint32_t h) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote_relaxed(tempty_leader + 8u * h);
+        };
+        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
             p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side, &tmOut,
-            &tmAux, &aw);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tempty_leader);
+            &tmAux, &aw, [&]() { release_half(0u); });
         if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
         // half 1 is complete a few k-slices after half 0
         bool ok1 = mbar_wait_bounded(tfull0 + 8u, use, abort_flag, p.wait_limit_ns);
@@ -597,12 +625,9 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           break;
         }
         tc_fence_after();
-        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true>(
+        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
             p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane, red + 256 + c_sub,
-            stg, side + kSideHalf, &tmOut, &tmAux, &aw);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(tempty_leader + 8u);
+            stg, side + kSideHalf, &tmOut, &tmAux, &aw, [&]() { release_half(1u); });
         if constexpr (EPI == EPI_RELU_AUX_BIAS)
           store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
       } else if constexpr (C::kEpiWarps == 8) {
@@ -616,7 +641,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       } else {
         constexpr bool kStg = pair_stg(EPI, false);
         epilogue_drain<EPI, T, BN, BN, kStg, false, kRing>(
-            p, t_row, row0, n0, q, lane, red, stg0 + 2048u * (uint32_t)(warp - 2), sring);
+            p, t_row, row0, n0, q, lane, red, stg0 + 2048u * (uint32_t)ew, sring);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);

@@ -313,6 +313,15 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                : "memory");
 }
 
+// The same arrive without release semantics: for a signal that orders no
+// memory accesses of this thread (e.g. an accumulator whose tensor-memory
+// reads have completed, tcgen05.wait::ld, before the arrive). It does not wait
+// for the thread's outstanding global or bulk stores.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -502,6 +511,21 @@ __device__ __forceinline__ void bulk_wait_all() {
 // make this thread's shared-memory writes visible to the tensor (async) proxy
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Per-warpgroup register reconfiguration: every warp of a warpgroup (4
+// consecutive warps) executes the same one. dec releases registers to the
+// CTA's pool; inc waits until the pool holds enough, so the warpgroups'
+// targets must add up to no more than the registers the CTA was launched
+// with (threads x registers per thread).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // named barrier over `count` threads (id 0 is __syncthreads)
