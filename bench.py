@@ -1076,6 +1076,13 @@ def run_swiglu_workload(args, gf, torch, dev, sp, pk, pk_kind, Ms):
                                     gf.GF_B_NK)
         dh_none = gf.gf_matmul_plan_ex(Mw, I, H, gf.GF_BF16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
                                        gf.GF_B_KN)
+        # the bare GEMMs run in the fused plans' kernel and tile configuration
+        for a, b in ((bare, fwd), (dh_none, bwd)):
+            d = gf.gf_plan_describe(b)
+            kern = (3 if d["tile_n"] == 512 else 2) if d["tile_m"] == 256 else 1
+            gf.gf_plan_set_option(a, gf.GF_OPT_KERNEL, kern)
+            if d["tile_m"] != 256:
+                gf.gf_plan_set_option(a, gf.GF_OPT_TILE_N, d["tile_n"])
         plans = (fwd, down, bwd, bare, dh_none)
 
         def t_gateup():

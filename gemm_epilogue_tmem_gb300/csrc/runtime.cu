@@ -211,17 +211,21 @@ void plan_tiles(gf_plan* p) {
   // single-CTA tile; take it when its tiles fill the resident pairs, else the
   // single-CTA kernel with the tile width that keeps the SMs busy.
   // Wide pair tiles (256 x 512) need 3/4 of the operand bytes per flop of
-  // the 256 x 256 pair tile but expose part of each epilogue (a few thousand
-  // cycles per tile): the plan takes them when a tile's mainloop is long
-  // (k >= 8192) and their coarser waves cost no more than 3 % of the
-  // 256 x 256 schedule; one B operand only.
+  // the 256 x 256 pair tile, whose mainloop the L2 side of the operand
+  // stream holds to ~85 % of the tensor rate, and they release each
+  // accumulator half as soon as it is in registers. The plan takes them
+  // when a tile's mainloop is long enough to cover a drain (k >= 2048) and
+  // their coarser waves, at the wide tile's higher efficiency, cost no more
+  // than the 256 x 256 schedule (measured on the GELU and SwiGLU shapes:
+  // 1.4-9 % faster, except where the wide waves quantise worse, e.g. 80
+  // tiles on 76 pairs); one B operand only.
   const int64_t m2 = (p->m + 255) / 256;
   const int64_t tiles256 = m2 * ((p->n + (dual ? 127 : 255)) / (dual ? 128 : 256));
   const int64_t tiles512 = m2 * ((p->n + 511) / 512);
   const int64_t cl = p->max_pair_clusters > 0 ? p->max_pair_clusters : 1;
   const bool wide_fits = !dual && p->max_pair_clusters > 0;
-  const bool wide_pays = wide_fits && p->k >= 8192 &&
-                         100 * 2 * ((tiles512 + cl - 1) / cl) <= 103 * ((tiles256 + cl - 1) / cl);
+  const bool wide_pays = wide_fits && p->k >= 2048 &&
+                         100 * 2 * ((tiles512 + cl - 1) / cl) <= 112 * ((tiles256 + cl - 1) / cl);
   const bool wide = wide_fits && (p->forced_kernel == 3 || (p->forced_kernel == 0 && wide_pays));
   const int pair_n = wide ? 512 : (dual ? 128 : 256);
   const int64_t pair_tiles = wide ? tiles512 : tiles256;

@@ -228,7 +228,7 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          GF_ERR_DEVICE_TIMEOUT from gf_plan_status. 0: off.
  * GF_OPT_KERNEL          : 0 the plan's choice (the CTA-pair kernel when its
  *                          256-row tiles fill the resident pairs, with
- *                          256 x 512 tiles when k >= 8192 and their waves
+ *                          256 x 512 tiles when k >= 2048 and their waves
  *                          quantise no worse; else the single-CTA kernel),
  *                          1 the single-CTA kernel
  *                          (128 x tile_n tiles), 2 the CTA-pair kernel
@@ -236,7 +236,8 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          it cannot be resident on this device), 3 the
  *                          CTA-pair kernel with 256 x 512 tiles (3/4 of the
  *                          operand traffic per flop, one accumulator whose
- *                          epilogue is partly exposed; not for the SwiGLU
+ *                          halves are released as soon as the epilogue has
+ *                          them in registers; not for the gate+up SwiGLU
  *                          plans: GF_ERR_UNSUPPORTED).
  * Returns GF_ERR_INVALID_VALUE for an unknown option or value.
  */
