@@ -35,7 +35,7 @@ template <int EPI, typename T, bool B_MN, bool WIDE = false>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
   auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE>;
   using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE),
-                    pair_stg(EPI, WIDE), pair_side_ring(EPI, WIDE)>;
+                    pair_stg(EPI, WIDE), pair_side_ring(EPI, WIDE), pair_stg2(EPI, WIDE)>;
   constexpr int smem = C::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {

@@ -195,13 +195,15 @@ __device__ __forceinline__ void store_rows32_staged(T* base, int M, int N, int r
 // lane 0 and tracked by its bulk groups; the buffer is written again only
 // after that store has read it. Nothing of it is left in flight for a later
 // release fence of the warp to wait for. Called by all 32 lanes.
-template <typename T>
+// PEND: bulk groups that may still be reading (0; 1 when the warp alternates
+// two staging buffers, each store waiting only for the one before the last).
+template <typename T, int PEND = 0>
 __device__ __forceinline__ void store_rows32_tma(const CUtensorMap* map, int row0w, int col0,
                                                  const float* v, uint32_t lane, uint32_t stg) {
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = pack2<T>(v[2 * i], v[2 * i + 1]);
-  if (lane == 0) bulk_wait_read_all();  // the previous store from this buffer has read it
+  if (lane == 0) bulk_wait_read<PEND>();  // the previous store from this buffer has read it
   __syncwarp();
   const uint32_t sw = (lane >> 1) & 3u;
 #pragma unroll
@@ -378,7 +380,8 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
                                                const CUtensorMap* tm_out = nullptr,
                                                const CUtensorMap* tm_aux = nullptr,
                                                AuxWords* words = nullptr,
-                                               Release release = Release()) {
+                                               Release release = Release(),
+                                               uint32_t stg2 = 0) {
   static_assert(!TMA || (STG && BN <= 128), "TMA-store drains: staged, at most 4 chunks");
   static_assert(!PRELOAD || (TMA && !epi_dual(EPI) && SRING == 0 && BN == 128),
                 "preloaded drains: TMA stores, one operand, 4 chunks");
@@ -411,9 +414,16 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   }
 
   // one 32 x 32 block of a 16-bit output: `aux` selects aux_out over out
+  // stg2 != 0 (TMA): out leaves through the second staging buffer, aux_out
+  // and the saved activations' transposes through the first, and a buffer
+  // waits only for the store before the last one
+  const bool two_stg = TMA && stg2 != 0;
   auto emit = [&](bool aux, int col0, const float* vals) {
     if constexpr (TMA) {
-      store_rows32_tma<T>(aux ? tm_aux : tm_out, row0w, col0, vals, lane, stg);
+      if (two_stg)
+        store_rows32_tma<T, 1>(aux ? tm_aux : tm_out, row0w, col0, vals, lane, aux ? stg : stg2);
+      else
+        store_rows32_tma<T>(aux ? tm_aux : tm_out, row0w, col0, vals, lane, stg);
     } else {
       emit_row32<T, STG>(reinterpret_cast<T*>(aux ? p.aux_out : p.out), p.M, p.N, row0w, col0,
                          vals, lane, stg);
@@ -481,7 +491,12 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   auto side_to_rows = [&](const uint4 (&sd)[kSideN], uint4 (&cur)[kSideN]) {
     if constexpr (kCoalesced) {
       if constexpr (TMA) {
-        if (lane == 0) bulk_wait_read_all();  // a TMA store may still be reading it
+        if (lane == 0) {  // a TMA store may still be reading it
+          if (two_stg)
+            bulk_wait_read<1>();
+          else
+            bulk_wait_read<0>();
+        }
         __syncwarp();
       }
 #pragma unroll

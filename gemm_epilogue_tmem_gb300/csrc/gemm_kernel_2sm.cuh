@@ -68,13 +68,19 @@ GF_HD constexpr int pair_side_ring(int epi, bool wide) {
   return !wide && epi == EPI_DSWIGLU ? 3 : 0;
 }
 
+// A second 2 KB staging buffer per epilogue warp (in place of the 1 KB
+// side-input buffer, which the dSwiGLU epilog does not use): the wide tiles'
+// dSwiGLU drain stores d_up from one buffer and d_gate from the other, so
+// that its two TMA stores per chunk do not wait for each other.
+GF_HD constexpr bool pair_stg2(int epi, bool wide) { return wide && epi == EPI_DSWIGLU; }
+
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
 // side in one accumulator); RED = the epilog reduces a bias gradient and
 // needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only); EPI8 =
 // eight epilogue warps (pair_epi8); SRING = side-input ring slots per
 // epilogue warp (pair_side_ring).
 template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE, bool STG = WIDE,
-          int SRING = 0>
+          int SRING = 0, bool STG2 = false>
 struct PairCfg {
   static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
   static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
@@ -115,7 +121,7 @@ struct PairCfg {
   // 2 x 128 columns)
   // (+ the side-input ring of SRING 4 KB chunk slots per warp)
   static constexpr int kStgBytes =
-      WIDE ? kEpiWarps * (2048 + 1024)
+      WIDE ? kEpiWarps * (2048 + (STG2 ? 2048 : 1024))
            : (STG ? kEpiWarps * (2048 + SRING * static_cast<int>(kSideSlotBytes)) : 0);
   static constexpr int kStages = ring_stages(kABytes + kStageBBytes, kRedBytes + kStgBytes);
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
@@ -170,7 +176,8 @@ __device__ __forceinline__ void store_aux_words(const GemmParams& p, int row0w, 
 template <int EPI, typename T, bool B_MN, bool WIDE = false>
 __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
                                           pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
-                                          pair_side_ring(EPI, WIDE)>::kThreads,
+                                          pair_side_ring(EPI, WIDE),
+                                          pair_stg2(EPI, WIDE)>::kThreads,
                                   1)
     gemm_epilog_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
                             const __grid_constant__ CUtensorMap tmAux, const GemmParams p) {
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
   using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
-                    pair_side_ring(EPI, WIDE)>;
+                    pair_side_ring(EPI, WIDE), pair_stg2(EPI, WIDE)>;
   constexpr int kRing = pair_side_ring(EPI, WIDE);
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
@@ -604,6 +611,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         // words are stored after the release, so that the release (a
         // cluster-scope release) has no global stores to wait for.
         const uint32_t stg = stg0 + 2048u * (uint32_t)ew;
+        // dSwiGLU: d_gate's staging buffer (in place of the side buffer)
+        const uint32_t stg2 = pair_stg2(EPI, WIDE) ? side0 + 2048u * (uint32_t)ew : 0u;
         AuxWords aw;
         // (a relaxed arrive: the accumulator's reads have completed before
         // it, and it must not wait for this warp's TMA stores in flight)
@@ -614,7 +623,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         };
         epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
             p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side, &tmOut,
-            &tmAux, &aw, [&]() { release_half(0u); });
+            &tmAux, &aw, [&]() { release_half(0u); }, stg2);
         if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
         // half 1 is complete a few k-slices after half 0
         bool ok1 = mbar_wait_bounded(tfull0 + 8u, use, abort_flag, p.wait_limit_ns);
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         tc_fence_after();
         epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
             p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane, red + 256 + c_sub,
-            stg, side + kSideHalf, &tmOut, &tmAux, &aw, [&]() { release_half(1u); });
+            stg, side + kSideHalf, &tmOut, &tmAux, &aw, [&]() { release_half(1u); }, stg2);
         if constexpr (EPI == EPI_RELU_AUX_BIAS)
           store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
       } else if constexpr (C::kEpiWarps == 8) {
