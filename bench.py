@@ -42,7 +42,7 @@ FALLBACK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6
 
 
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles",
-                               "linear_pair_fp16_65536x16384x8192_dram_traffic.md")
+                               "gemm_epilog_pair_kernel_wide_fp16_16384_rows_dram_traffic.md")
 
 
 def kernel_sources_sha256() -> str:
