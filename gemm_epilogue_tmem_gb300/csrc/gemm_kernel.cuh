@@ -367,21 +367,29 @@ __device__ __forceinline__ void side_ring_prefetch(const GemmParams& p, int row0
 // is called -- the accumulator may be overwritten from then on -- and the
 // chunks are processed from registers. The MMAs that wait for this
 // accumulator then wait only for its tensor-memory reads, not for the
-// epilogue's arithmetic and stores.
+// epilogue's arithmetic and stores. With PRELOAD the drain also waits for
+// the accumulator itself (`wait_acc`, false: the wait gave up, nothing is
+// drained and the drain returns false), after issuing the first chunk's
+// side-input loads, so that their latency runs under the end of the
+// mainloop instead of at the start of the drain.
 struct NoRelease {
   __device__ __forceinline__ void operator()() const {}
 };
+struct NoWait {
+  __device__ __forceinline__ bool operator()() const { return true; }
+};
 
 template <int EPI, typename T, int BN, int RS = BN, bool STG = false, bool SIDE = false,
-          int SRING = 0, bool TMA = false, bool PRELOAD = false, typename Release = NoRelease>
-__device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
+          int SRING = 0, bool TMA = false, bool PRELOAD = false, typename Release = NoRelease,
+          typename WaitAcc = NoWait>
+__device__ __forceinline__ bool epilogue_drain(const GemmParams& p, uint32_t t_row, int row0,
                                                int n0, int q, uint32_t lane, float* red,
                                                uint32_t stg = 0, uint32_t side = 0,
                                                const CUtensorMap* tm_out = nullptr,
                                                const CUtensorMap* tm_aux = nullptr,
                                                AuxWords* words = nullptr,
                                                Release release = Release(),
-                                               uint32_t stg2 = 0) {
+                                               uint32_t stg2 = 0, WaitAcc wait_acc = WaitAcc()) {
   static_assert(!TMA || (STG && BN <= 128), "TMA-store drains: staged, at most 4 chunks");
   static_assert(!PRELOAD || (TMA && !epi_dual(EPI) && SRING == 0 && BN == 128),
                 "preloaded drains: TMA stores, one operand, 4 chunks");
@@ -409,8 +417,11 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
   static_assert(!kRing || (STG && EPI == EPI_DSWIGLU), "side ring: dSwiGLU with staging");
   if (nch <= 0) {
     if constexpr (kRing) cp_async_wait_all();
-    if constexpr (PRELOAD) release();
-    return;
+    if constexpr (PRELOAD) {
+      if (!wait_acc()) return false;
+      release();
+    }
+    return true;
   }
 
   // one 32 x 32 block of a 16-bit output: `aux` selects aux_out over out
@@ -634,8 +645,11 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
 
   uint4 sd[kSideN];
   if constexpr (PRELOAD) {
-    // every chunk out of tensor memory (BN registers per thread), then the
+    // the first chunk's side inputs in flight, then the accumulator; every
+    // chunk of it out of tensor memory (BN registers per thread), and the
     // accumulator is free again
+    load_side(n0, sd);
+    if (!wait_acc()) return false;
     uint32_t pre[BN / 32][32];
     float u2[1];
     if (has_acc) {
@@ -651,7 +665,6 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
         for (int j = 0; j < 32; ++j) pre[c][j] = 0u;  // nothing multiplied: zero
     }
     release();
-    load_side(n0, sd);
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
       if (c < nch) {
@@ -664,7 +677,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
         finish_chunk(c, v, u2, cur);
       }
     }
-    return;
+    return true;
   }
 
   uint32_t ra[32];
@@ -725,6 +738,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmParams& p, uint32_t t_r
     }
     finish_chunk(c, v, u2, cur);
   }
+  return true;
 }
 
 // Column sums of the tile's 128 rows: the four warps' 32-row sums (in red,

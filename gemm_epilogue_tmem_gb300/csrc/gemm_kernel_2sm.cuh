@@ -593,14 +593,21 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
                                      lane, sring);
       const int buf = WIDE ? 0 : (it & 1);
       const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
-      ok = mbar_wait_bounded(tfull0 + 8u * buf, use, abort_flag, p.wait_limit_ns);
-      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, NT, !ok);
-      if (!ok) {
+      // the accumulator (wide: accumulator half h) is complete; all epilogue
+      // warps take part (the bias-gradient epilogs agree on the outcome)
+      auto wait_acc = [&](uint32_t h) -> bool {
+        bool okh = mbar_wait_bounded(tfull0 + 8u * (buf + h), use, abort_flag, p.wait_limit_ns);
+        if constexpr (epi_has_bgrad(EPI)) okh = !named_bar_red_or(1, NT, !okh);
+        if (okh) tc_fence_after();
+        return okh;
+      };
+      // (wide: each half's drain waits for its half itself, after issuing
+      // the loads of its first side inputs)
+      if (!WIDE && !wait_acc(0u)) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
         aborted = true;
         break;
       }
-      tc_fence_after();
       const uint32_t t_row =
           tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::kAccCols);
       if constexpr (WIDE) {
@@ -621,22 +628,24 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           __syncwarp();
           if (lane == 0) mbar_arrive_remote_relaxed(tempty_leader + 8u * h);
         };
-        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
-            p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side, &tmOut,
-            &tmAux, &aw, [&]() { release_half(0u); }, stg2);
-        if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
-        // half 1 is complete a few k-slices after half 0
-        bool ok1 = mbar_wait_bounded(tfull0 + 8u, use, abort_flag, p.wait_limit_ns);
-        if constexpr (epi_has_bgrad(EPI)) ok1 = !named_bar_red_or(1, NT, !ok1);
-        if (!ok1) {
+        if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
+                p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side,
+                &tmOut, &tmAux, &aw, [&]() { release_half(0u); }, stg2,
+                [&]() { return wait_acc(0u); })) {
           raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
           aborted = true;
           break;
         }
-        tc_fence_after();
-        epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
-            p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane, red + 256 + c_sub,
-            stg, side + kSideHalf, &tmOut, &tmAux, &aw, [&]() { release_half(1u); }, stg2);
+        if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
+        // half 1 is complete a few k-slices after half 0
+        if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
+                p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane,
+                red + 256 + c_sub, stg, side + kSideHalf, &tmOut, &tmAux, &aw,
+                [&]() { release_half(1u); }, stg2, [&]() { return wait_acc(1u); })) {
+          raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+          aborted = true;
+          break;
+        }
         if constexpr (EPI == EPI_RELU_AUX_BIAS)
           store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
       } else if constexpr (C::kEpiWarps == 8) {
