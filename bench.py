@@ -116,6 +116,7 @@ class ClockSampler:
         self.gpu = gpu
         self.proc = None
         self.lines: list[str] = []
+        self.times: list[float] = []  # time.monotonic() when each sample arrived
 
     def start(self):
         try:
@@ -130,9 +131,17 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
+            self.times.append(time.monotonic())
             self.lines.append(line.strip())
 
-    def stop(self) -> dict:
+    def keep_from(self, n: int):
+        """Drop the first n samples."""
+        self.lines, self.times = self.lines[n:], self.times[n:]
+
+    def stop(self, window=None) -> dict:
+        """Median clock, power and the throttle reasons seen, over the samples
+        that arrived within window = (t0, t1) of time.monotonic() (all
+        samples when None)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -142,7 +151,9 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln, t in zip(self.lines, self.times):
+            if window is not None and not window[0] <= t <= window[1]:
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -155,10 +166,17 @@ class ClockSampler:
             for nm, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_median": statistics.median(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "power_w_median": statistics.median(power) if power else None,
+               "samples": len(sm), "reasons": sorted(reasons)}
+        if window is not None:
+            out["sampled"] = "only while the timed loop ran"
+            if not sm:
+                out["note"] = ("the timed region (%.0f ms) is shorter than the 200 ms sampling "
+                               "interval; the steady-state comparison has sampled clocks"
+                               % (1e3 * (window[1] - window[0])))
+        return out
 
 
 def pick_peak(pk: dict, pk_kind: str, busy_s: float):
@@ -481,12 +499,13 @@ def run_gpu(args):
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    h0 = time.monotonic()
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     t_end.record(stream)
     barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(window=(h0, time.monotonic()))
     status_ok = gf.gf_plan_status(fwd, sp) == gf.GF_OK and gf.gf_plan_status(bwd, sp) == gf.GF_OK
     ms_total = t_start.elapsed_time(t_end)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -897,6 +916,7 @@ def _timed_steps(torch, step_fns: dict, steps: int, warmup: int, gpu: int) -> di
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     s = torch.cuda.current_stream()
+    h0 = time.monotonic()
     t0.record(s)
     for i in range(steps):
         for j, fn in enumerate(step_fns.values()):
@@ -905,7 +925,7 @@ def _timed_steps(torch, step_fns: dict, steps: int, warmup: int, gpu: int) -> di
         evs[i][-1].record(s)
     t1.record(s)
     torch.cuda.synchronize()
-    clk = sampler.stop()
+    clk = sampler.stop(window=(h0, time.monotonic()))
     per = {n: stats_ms([e[j].elapsed_time(e[j + 1]) for e in evs]) for j, n in enumerate(names)}
     return {"ms_total": t0.elapsed_time(t1), "per_kernel": per, "clocks": clk}
 
@@ -1449,7 +1469,7 @@ def run_compare_schedules(args):
             b.record()
             b.synchronize()
             times.append(a.elapsed_time(b))
-        sampler.lines = sampler.lines[n0:]
+        sampler.keep_from(n0)
         clk = sampler.stop()
         ms = statistics.median(times)
         return {"ms": ms, "tflops": FLOP_PER_GEMM / (ms * 1e-3) / 1e12, "sm_mhz": clk["sm_mhz"],

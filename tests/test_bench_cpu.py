@@ -73,3 +73,34 @@ def test_stats_and_parity_block():
     assert not bench._parity_block({"Y": {"nmax": 0.0, "rel_l2": 0.0}},
                                    mask={"mask_mismatch_outside_band": 1,
                                          "mask_mismatch_in_band": 0})["pass"]
+
+
+class _Done:
+    """Stands in for the finished nvidia-smi process."""
+
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sample(mhz, power, cap):
+    return f"0, {mhz}, 2070, {power}, 0x4, Not Active, Not Active, Not Active, {cap}"
+
+
+def test_clock_samples_outside_the_timed_region_are_left_out():
+    s = bench.ClockSampler(0)
+    s.proc = _Done()
+    s.lines = [_sample(2070, 160, "Not Active"), _sample(1400, 1370, "Active"),
+               _sample(1420, 1375, "Active"), _sample(2070, 170, "Not Active")]
+    s.times = [10.0, 10.5, 10.7, 11.2]
+    c = s.stop(window=(10.4, 11.0))
+    assert c["samples"] == 2 and c["sm_mhz"] == 1410.0 and c["reasons"] == ["sw_power_cap"]
+    assert "note" not in c
+    c = s.stop(window=(10.55, 10.65))  # no sample inside: say so instead of idle clocks
+    assert c["samples"] == 0 and c["sm_mhz"] is None and "200 ms" in c["note"]
+    c = s.stop()  # no window: every sample
+    assert c["samples"] == 4 and c["sm_mhz"] == 1745.0
+    s.keep_from(2)
+    assert s.lines[0].startswith("0, 1420") and s.times == [10.7, 11.2]
