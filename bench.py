@@ -1100,9 +1100,11 @@ def run_swiglu_workload(args, gf, torch, dev, sp, pk, pk_kind, Ms):
         dh_none = gf.gf_matmul_plan_ex(Mw, I, H, gf.GF_BF16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
                                        gf.GF_B_KN)
         # the bare GEMMs run in the fused plans' kernel and tile configuration
-        for a, b in ((bare, fwd), (dh_none, bwd)):
+        # (the gate+up kernel's tiles are half as wide as the bare GEMM's of
+        # [Wg; Wu]: each output column takes a column of both operands)
+        for a, b, wide_n in ((bare, fwd, 256), (dh_none, bwd, 512)):
             d = gf.gf_plan_describe(b)
-            kern = (3 if d["tile_n"] == 512 else 2) if d["tile_m"] == 256 else 1
+            kern = (3 if d["tile_n"] == wide_n else 2) if d["tile_m"] == 256 else 1
             gf.gf_plan_set_option(a, gf.GF_OPT_KERNEL, kern)
             if d["tile_m"] != 256:
                 gf.gf_plan_set_option(a, gf.GF_OPT_TILE_N, d["tile_n"])

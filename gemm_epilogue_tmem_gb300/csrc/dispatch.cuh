@@ -97,9 +97,13 @@ int pair_max_clusters() {
 }
 
 // two-B-operand epilogs: B given [n, k] (K-major), 128-wide single-CTA tiles or CTA pairs
+// (256 x 128 tiles, or 256 x 256 wide tiles)
 template <int EPI>
 cudaError_t launch_dual(const LaunchArgs& a) {
-  if (a.b_mn || a.wide) return cudaErrorInvalidValue;
+  if (a.b_mn) return cudaErrorInvalidValue;
+  if (a.pair && a.wide)
+    return a.bf16 ? launch_pair_instance<EPI, __nv_bfloat16, false, true>(a)
+                  : launch_pair_instance<EPI, __half, false, true>(a);
   if (a.pair)
     return a.bf16 ? launch_pair_instance<EPI, __nv_bfloat16, false>(a)
                   : launch_pair_instance<EPI, __half, false>(a);

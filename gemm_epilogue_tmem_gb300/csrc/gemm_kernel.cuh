@@ -741,6 +741,65 @@ __device__ __forceinline__ bool epilogue_drain(const GemmParams& p, uint32_t t_r
   return true;
 }
 
+// One warp's share of an accumulator half of the two-operand wide tile
+// (gate+up SwiGLU): g of 64 output columns from n0 at t_g, u of the same
+// columns at t_u, rows row0 + 32 q + lane. Waits for the half (`wait_acc`,
+// false: the wait gave up, nothing is drained), loads both 64-column pieces
+// into registers, releases the half, then per 32-column chunk stores g and u
+// (SWIGLU_SAVE, through the staging buffer) and h = silu(g) * u (a TMA store
+// from the staging buffer) -- the same arithmetic as the drain of the 256 x
+// 128 two-operand tile.
+template <int EPI, typename T, typename Release, typename WaitAcc>
+__device__ __forceinline__ bool epilogue_drain_dual_wide(const GemmParams& p, uint32_t t_g,
+                                                         uint32_t t_u, int row0, int n0, int q,
+                                                         uint32_t lane, uint32_t stg,
+                                                         const CUtensorMap* tm_out,
+                                                         Release release, WaitAcc wait_acc) {
+  const int row0w = row0 + 32 * q;
+  const int nch = min(2, (p.N - n0 + 31) / 32);  // chunks with columns below N
+  if (!wait_acc()) return false;
+  uint32_t pre[4][32];  // g chunk 0, g chunk 1, u chunk 0, u chunk 1
+  if (p.num_k_blocks > 0 && nch > 0) {
+    tmem_ld_32x32b_x32(t_g, pre[0]);
+    tmem_ld_32x32b_x32(t_g + 32u, pre[1]);
+    tmem_ld_32x32b_x32(t_u, pre[2]);
+    tmem_ld_32x32b_x32(t_u + 32u, pre[3]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_tie(pre[c]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pre[c][j] = 0u;  // nothing multiplied: zero
+  }
+  release();
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (c < nch) {
+      const int col0 = n0 + 32 * c;
+      float g[32], u[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = __uint_as_float(pre[c][j]);
+        u[j] = __uint_as_float(pre[2 + c][j]);
+      }
+      if constexpr (EPI == EPI_SWIGLU_SAVE) {
+        if (lane == 0) bulk_wait_read<0>();  // the last h store has read the buffer
+        __syncwarp();
+        store_rows32_staged<T>(reinterpret_cast<T*>(p.aux_out), p.M, p.N, row0w, col0, g, lane,
+                               stg);
+        store_rows32_staged<T>(reinterpret_cast<T*>(p.aux_out2), p.M, p.N, row0w, col0, u, lane,
+                               stg);
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = silu_f(g[j]) * u[j];
+      store_rows32_tma<T>(tm_out, row0w, col0, g, lane, stg);
+    }
+  }
+  return true;
+}
+
 // Column sums of the tile's 128 rows: the four warps' 32-row sums (in red,
 // [4][BN]) added in a fixed order, then one partial per 128-row block or one
 // atomicAdd per column. Called by the NT epilogue threads (ep_tid 0..NT-1).

@@ -38,6 +38,9 @@
 //     ring of k-slices into half 0 first so that half 0's drain starts early.
 //     Eight epilogue warps (two per TMEM lane quarter, each with half of the
 //     columns) keep that exposed drain short.
+//     With two B operands (gate+up SwiGLU) a wide tile is 256 x 256 outputs:
+//     each CTA loads two 128-row parts of its own weight, so accumulator half
+//     h holds g and u of output columns 128 h .. 128 h + 127 side by side.
 //   - Teardown: drains, then a cluster barrier, then a pair TMEM dealloc.
 #pragma once
 
@@ -76,14 +79,15 @@ GF_HD constexpr bool pair_stg2(int epi, bool wide) { return wide && epi == EPI_D
 
 // NB = number of B operands: 1, or 2 for the gate+up SwiGLU (g and u side by
 // side in one accumulator); RED = the epilog reduces a bias gradient and
-// needs the [4][BN] scratch; WIDE = 256 x 512 tiles (NB = 1 only); EPI8 =
+// needs the [4][BN] scratch; WIDE = two N = 256 MMAs per k-step into one
+// 512-column accumulator (256 x 512 tiles; 256 x 256 with two B operands); EPI8 =
 // eight epilogue warps (pair_epi8); SRING = side-input ring slots per
 // epilogue warp (pair_side_ring).
 template <int NB = 1, bool RED = false, bool WIDE = false, bool EPI8 = WIDE, bool STG = WIDE,
           int SRING = 0, bool STG2 = false>
 struct PairCfg {
-  static_assert(!WIDE || NB == 1, "wide tiles have one B operand");
-  static constexpr int BN = WIDE ? 512 : (NB == 2 ? 128 : 256);  // output columns of a tile
+  // output columns of a tile
+  static constexpr int BN = WIDE ? (NB == 2 ? 256 : 512) : (NB == 2 ? 128 : 256);
   static constexpr int kABytes = kBM * kBK * 2;        // 16 KB: this CTA's 128 rows of A
   // one 16 KB B part: this CTA's 128 of an MMA's 256 B columns, or (two
   // operands) the tile's 128 columns of this CTA's operand; wide: two parts
@@ -366,7 +370,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
 #pragma unroll
             for (int h = 0; h < (WIDE ? 2 : 1); ++h) {
               const uint32_t dst = sB + stage * C::kStageBBytes + h * C::kBPartBytes;
-              const int col = n_col + 256 * h;
+              // (two operands: part h is output columns 128 h of the tile)
+              const int col = n_col + (NB == 2 ? 128 : 256) * h;
               if (B_MN && p.b_mn_3d) {
                 tma_load3_pair(dst, &tmB, fb, 0, kb * kBK, col / 64, hb, pol_b);
               } else if (B_MN) {
@@ -628,26 +633,46 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           __syncwarp();
           if (lane == 0) mbar_arrive_remote_relaxed(tempty_leader + 8u * h);
         };
-        if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
-                p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side,
-                &tmOut, &tmAux, &aw, [&]() { release_half(0u); }, stg2,
-                [&]() { return wait_acc(0u); })) {
-          raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
-          aborted = true;
-          break;
+        if constexpr (NB == 2) {
+          // two operands: half h holds g (columns 0..127) and u (128..255) of
+          // output columns n0 + 128 h ..; this warp takes 64 of them
+          const uint32_t c64 = 64u * (uint32_t)sub;
+          if (!epilogue_drain_dual_wide<EPI, T>(
+                  p, t_row + c64, t_row + 128u + c64, row0, n0 + (int)c64, q, lane, stg, &tmOut,
+                  [&]() { release_half(0u); }, [&]() { return wait_acc(0u); })) {
+            raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+            aborted = true;
+            break;
+          }
+          if (!epilogue_drain_dual_wide<EPI, T>(
+                  p, t_row + 256u + c64, t_row + 384u + c64, row0, n0 + 128 + (int)c64, q, lane,
+                  stg, &tmOut, [&]() { release_half(1u); }, [&]() { return wait_acc(1u); })) {
+            raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+            aborted = true;
+            break;
+          }
+        } else {
+          if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
+                  p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side,
+                  &tmOut, &tmAux, &aw, [&]() { release_half(0u); }, stg2,
+                  [&]() { return wait_acc(0u); })) {
+            raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+            aborted = true;
+            break;
+          }
+          if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
+          // half 1 is complete a few k-slices after half 0
+          if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
+                  p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane,
+                  red + 256 + c_sub, stg, side + kSideHalf, &tmOut, &tmAux, &aw,
+                  [&]() { release_half(1u); }, stg2, [&]() { return wait_acc(1u); })) {
+            raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+            aborted = true;
+            break;
+          }
+          if constexpr (EPI == EPI_RELU_AUX_BIAS)
+            store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
         }
-        if constexpr (EPI == EPI_RELU_AUX_BIAS) store_aux_words(p, row0 + 32 * q, n0 + c_sub, lane, aw);
-        // half 1 is complete a few k-slices after half 0
-        if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
-                p, t_row + 256u + (uint32_t)c_sub, row0, n0 + 256 + c_sub, q, lane,
-                red + 256 + c_sub, stg, side + kSideHalf, &tmOut, &tmAux, &aw,
-                [&]() { release_half(1u); }, stg2, [&]() { return wait_acc(1u); })) {
-          raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
-          aborted = true;
-          break;
-        }
-        if constexpr (EPI == EPI_RELU_AUX_BIAS)
-          store_aux_words(p, row0 + 32 * q, n0 + 256 + c_sub, lane, aw);
       } else if constexpr (C::kEpiWarps == 8) {
         // this warp's half of the tile's columns
         constexpr int H = BN / 2;

@@ -9,6 +9,7 @@ cudaError_t launch_none_bias(int epi, const LaunchArgs& a) {
 
 int stages_for(int tile_n, int pair, int epi) {
   const bool red = epi_has_bgrad(epi);
+  if (epi_dual(epi) && pair && tile_n == 256) return PairCfg<2, false, true>::kStages;
   if (epi_dual(epi) && pair)
     return pair_stg(epi, false) ? PairCfg<2, false, false, false, true>::kStages
                                 : PairCfg<2, false>::kStages;

@@ -218,16 +218,20 @@ void plan_tiles(gf_plan* p) {
   // their coarser waves, at the wide tile's higher efficiency, cost no more
   // than the 256 x 256 schedule (measured on the GELU and SwiGLU shapes:
   // 1.4-9 % faster, except where the wide waves quantise worse, e.g. 80
-  // tiles on 76 pairs); one B operand only.
+  // tiles on 76 pairs). With two B operands the tiles are half as wide
+  // (256 x 128 and 256 x 256 outputs, each output column taking a column of
+  // both operands).
   const int64_t m2 = (p->m + 255) / 256;
-  const int64_t tiles256 = m2 * ((p->n + (dual ? 127 : 255)) / (dual ? 128 : 256));
-  const int64_t tiles512 = m2 * ((p->n + 511) / 512);
+  const int pair_n_narrow = dual ? 128 : 256;
+  const int pair_n_wide = dual ? 256 : 512;
+  const int64_t tiles256 = m2 * ((p->n + pair_n_narrow - 1) / pair_n_narrow);
+  const int64_t tiles512 = m2 * ((p->n + pair_n_wide - 1) / pair_n_wide);
   const int64_t cl = p->max_pair_clusters > 0 ? p->max_pair_clusters : 1;
-  const bool wide_fits = !dual && p->max_pair_clusters > 0;
+  const bool wide_fits = p->max_pair_clusters > 0;
   const bool wide_pays = wide_fits && p->k >= 2048 &&
                          100 * 2 * ((tiles512 + cl - 1) / cl) <= 112 * ((tiles256 + cl - 1) / cl);
   const bool wide = wide_fits && (p->forced_kernel == 3 || (p->forced_kernel == 0 && wide_pays));
-  const int pair_n = wide ? 512 : (dual ? 128 : 256);
+  const int pair_n = wide ? pair_n_wide : pair_n_narrow;
   const int64_t pair_tiles = wide ? tiles512 : tiles256;
   bool pair = false;
   if (p->forced_kernel == 2 || p->forced_kernel == 3)
@@ -540,8 +544,10 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
     if (p->k > 0) {
       if (!encode_2d(&tmA, x.A, p->dtype, p->k, p->m, 64, kBM)) return fail(GF_ERR_INVALID_VALUE);
       // K-major B boxes: a pair CTA loads half of the tile's columns, or with
-      // two B operands all of the tile's columns of one operand
-      const uint32_t rows_nk = p->pair && !dual ? 128u : static_cast<uint32_t>(p->tile_n);
+      // two B operands all of the tile's columns of one operand; the wide
+      // tiles load 128-row parts
+      const uint32_t rows_nk =
+          p->pair && (!dual || p->wide) ? 128u : static_cast<uint32_t>(p->tile_n);
       // MN-major B: one 3-D box per k-slice for all of this CTA's column
       // chunks when n is a multiple of 64, else one 2-D box per chunk
       b_mn_3d = p->b_layout == GF_B_KN && p->n % 64 == 0 &&
@@ -749,7 +755,6 @@ GF_API gf_status gf_plan_set_option(gf_plan* p, gf_option option, int64_t value)
     case GF_OPT_KERNEL:
       if (value < 0 || value > 3) return fail(GF_ERR_INVALID_VALUE);
       if (value >= 2 && p->max_pair_clusters == 0) return fail(GF_ERR_UNSUPPORTED);
-      if (value == 3 && gf::epi_dual(p->epi)) return fail(GF_ERR_UNSUPPORTED);
       p->forced_kernel = static_cast<int>(value);
       return replan(p) == GF_OK ? GF_OK : fail(GF_ERR_OUT_OF_MEMORY);
     case GF_OPT_L2_HINTS:

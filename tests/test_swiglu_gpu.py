@@ -28,7 +28,7 @@ def _weights(M, H, I, d, seed):
 
 @pytest.mark.parametrize("M,I,H", SHAPES)
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F16])
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_swiglu_forward(M, I, H, dtype, kernel):
     x, Wg, Wu = _weights(M, H, I, dtype, 3)
     tdt = torch_dtype(dtype)
@@ -52,7 +52,7 @@ def test_swiglu_forward(M, I, H, dtype, kernel):
 
 @pytest.mark.parametrize("M,I,H", SHAPES)
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F16])
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_dswiglu(M, I, H, dtype, kernel):
     dout = synth.normal((M, H), dtype, 4, synth.TID_DOUT, 1.0)
     Wd = synth.normal((H, I), dtype, 4, synth.TID_WD, 1 / np.sqrt(H))

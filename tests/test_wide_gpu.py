@@ -1,7 +1,8 @@
 """The CTA-pair kernel with 256 x 512 tiles (GF_OPT_KERNEL = 3): one
 512-column accumulator per pair, drained in two halves while the next tile
 starts on the first half and the last k-slices of a tile finish the first
-half early. Checked against the oracle on
+half early (with the two SwiGLU operands: 256 x 256 tiles). Checked against
+the oracle on
 ragged shapes (N not a multiple of 512 or of 64, K not a multiple of 64, fewer
 k-slices than ring stages, K = 0), on every epilog family it serves, with many
 tiles per CTA pair, under both schedules, and through a bounded wait that runs
@@ -146,11 +147,31 @@ def test_wide_dswiglu():
     assert_close(to_host_f32(du), oracle.decode(du_o, d), what="d_up")
 
 
-def test_wide_rejected_for_two_operands():
-    plan = gf.gf_swiglu_plan(1024, 1024, 256, synth.BF16)
-    with pytest.raises(gf.GfError):
-        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, WIDE)
-    plan.free()
+@pytest.mark.parametrize("save", [True, False])
+def test_wide_two_operands_same_bits(save):
+    """Gate+up SwiGLU on 256 x 256 wide tiles (each CTA loads two 128-row
+    parts of its weight) gives the same bits as on the 256 x 128 two-operand
+    tiles: every output sums its k-slices in the same order. Several tiles
+    per CTA pair, a ragged last column block."""
+    M, I, H = 4096, 8200, 2048
+    d = synth.BF16
+    x = to_dev(synth.normal((M, H), d, 49, synth.TID_A, 1.0), d)
+    Wg = to_dev(synth.normal((I, H), d, 49, synth.TID_WG, 0.02), d)
+    Wu = to_dev(synth.normal((I, H), d, 49, synth.TID_WU, 0.02), d)
+    outs = []
+    for kern in (2, WIDE):
+        h, g, u = (torch.full((M, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+                   for _ in range(3))
+        plan = gf.gf_swiglu_plan(M, I, H, d, save_gu=save)
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, kern)
+        dsc = gf.gf_plan_describe(plan)
+        assert (dsc["tile_m"], dsc["tile_n"]) == ((256, 256) if kern == WIDE else (256, 128)), dsc
+        gf.gf_swiglu_execute(plan, x, Wg, Wu, h, g if save else None, u if save else None)
+        assert gf.gf_plan_status(plan) == gf.GF_OK
+        plan.free()
+        outs.append((h, g, u) if save else (h,))
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 MT, NT, KT = 8192, 8192, 128  # 512 wide tiles: several per CTA pair
