@@ -232,13 +232,15 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          quantise no worse; else the single-CTA kernel),
  *                          1 the single-CTA kernel
  *                          (128 x tile_n tiles), 2 the CTA-pair kernel
- *                          (256 x 256 tiles on two SMs; GF_ERR_UNSUPPORTED if
- *                          it cannot be resident on this device), 3 the
- *                          CTA-pair kernel with 256 x 512 tiles (3/4 of the
+ *                          (256 x 256 tiles on two SMs, 256 x 128 for the
+ *                          gate+up SwiGLU plans; GF_ERR_UNSUPPORTED if it
+ *                          cannot be resident on this device), 3 the
+ *                          CTA-pair kernel with 256 x 512 tiles (256 x 256
+ *                          for the gate+up SwiGLU plans, each output column
+ *                          taking a column of both weights: 3/4 of the
  *                          operand traffic per flop, one accumulator whose
  *                          halves are released as soon as the epilogue has
- *                          them in registers; not for the gate+up SwiGLU
- *                          plans: GF_ERR_UNSUPPORTED).
+ *                          them in registers).
  * Returns GF_ERR_INVALID_VALUE for an unknown option or value.
  */
 typedef enum gf_option {
