@@ -124,6 +124,12 @@ typedef struct gf_plan gf_plan;
  *             GF_EPILOG_NONE.
  * Returns a library-owned plan (release with gf_plan_free), or NULL with the
  * reason in gf_last_error().
+ *
+ * Environment overrides, read when a plan is made (gf_plan_set_option
+ * called afterwards wins): GF_KERNEL (as GF_OPT_KERNEL), GF_TILE_N (128 or
+ * 256, as GF_OPT_TILE_N), GF_BGRAD_MODE=atomic, GF_WAIT_LIMIT_US (as
+ * GF_OPT_WAIT_LIMIT_US); GF_DEBUG prints a nonzero device status word from
+ * gf_plan_status on stderr. Out-of-range values are ignored.
  */
 GF_API gf_plan* gf_matmul_plan(int64_t m, int64_t n, int64_t k, gf_dtype dtype, gf_epilog epilog,
                                gf_bias_axis bias_axis);
