@@ -739,6 +739,8 @@ def run_profile_case(args):
     m, n, k = (int(x) for x in args.profile_case.split(","))
     if args.epilog in ("swiglu_save", "dswiglu"):
         return run_profile_case_swiglu(args, m, n, k)
+    if args.epilog in ("gelu_aux_bias", "dgelu_bgrad"):
+        return run_profile_case_gelu(args, m, n, k)
     epi = {"relu_aux_bias": gf.GF_EPILOG_RELU_AUX_BIAS, "drelu_bgrad": gf.GF_EPILOG_DRELU_BGRAD,
            "none": gf.GF_EPILOG_NONE, "relu_bias": gf.GF_EPILOG_RELU_BIAS}[args.epilog]
     layout = gf.GF_B_NK if epi == gf.GF_EPILOG_DRELU_BGRAD else gf.GF_B_KN
@@ -768,6 +770,53 @@ def run_profile_case(args):
             gf.gf_matmul_execute(plan, A, B, out=out, aux_in=aux, bgrad=bgrad, stream=sp)
         else:
             gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=aux, stream=sp)
+    torch.cuda.synchronize()
+    st = gf.gf_plan_status(plan, sp)
+    print(json.dumps({"profile_case": [m, n, k], "epilog": args.epilog, "status": st,
+                      "plan": gf.gf_plan_describe(plan)}))
+    plan.free()
+    return 0 if st == gf.GF_OK else 1
+
+
+def run_profile_case_gelu(args, m, n, k):
+    """--profile-case M,N,K with --epilog gelu_aux_bias (X[M,K] W[K,N], the
+    pre-activation saved in bf16) or dgelu_bgrad (dY[M,K] with W given [N,K],
+    the saved pre-activation [M,N] read back), bf16."""
+    import torch
+
+    import gemm_epilogue_tmem_gb300 as gf
+    gf.build()
+    synth.build_cuda()
+    sp = torch.cuda.current_stream().cuda_stream
+    bf = torch.bfloat16
+    dev = torch.device("cuda", 0)
+
+    def filled(shape, tid, sigma):
+        t = torch.empty(shape, dtype=bf, device=dev)
+        synth.dev_normal(t, synth.BF16, 0, tid, sigma, sp)
+        return t
+
+    out = torch.empty((m, n), dtype=bf, device=dev)
+    fwd = args.epilog == "gelu_aux_bias"
+    A = filled((m, k), synth.TID_A if fwd else synth.TID_DY, 1.0)
+    B = filled((k, n) if fwd else (n, k), synth.TID_B, 1 / np.sqrt(k))
+    if fwd:
+        bias, pre = filled((n,), synth.TID_BIAS, 0.1), torch.empty((m, n), dtype=bf, device=dev)
+        plan = gf.gf_matmul_plan_ex(m, n, k, gf.GF_BF16, gf.GF_EPILOG_GELU_AUX_BIAS,
+                                    gf.GF_BIAS_COL, gf.GF_B_KN)
+        fn = lambda: gf.gf_matmul_execute(plan, A, B, bias=bias, out=out, aux_out=pre,  # noqa: E731
+                                          stream=sp)
+    else:
+        pre, bgrad = filled((m, n), synth.TID_PREACT, 1.0), torch.empty((n,), dtype=torch.float32,
+                                                                        device=dev)
+        plan = gf.gf_matmul_plan_ex(m, n, k, gf.GF_BF16, gf.GF_EPILOG_DGELU_BGRAD,
+                                    gf.GF_BIAS_COL, gf.GF_B_NK)
+        fn = lambda: gf.gf_matmul_execute(plan, A, B, out=out, aux_in=pre,  # noqa: E731
+                                          bgrad=bgrad, stream=sp)
+    if args.kernel:
+        gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, args.kernel)
+    for _ in range(args.warmup + args.steps):
+        fn()
     torch.cuda.synchronize()
     st = gf.gf_plan_status(plan, sp)
     print(json.dumps({"profile_case": [m, n, k], "epilog": args.epilog, "status": st,
@@ -1497,7 +1546,7 @@ def main():
                     help="M,N,K: run one fused GEMM of this shape (for ncu captures)")
     ap.add_argument("--epilog", default="relu_aux_bias",
                     choices=["relu_aux_bias", "drelu_bgrad", "none", "relu_bias", "swiglu_save",
-                             "dswiglu"])
+                             "dswiglu", "gelu_aux_bias", "dgelu_bgrad"])
     ap.add_argument("--kernel", type=int, default=0,
                     help="0 plan's choice, 1 single CTA, 2 pair, 3 pair with 256 x 512 tiles")
     ap.add_argument("--l2-hints", type=int, default=-1,
