@@ -1,7 +1,8 @@
 """Tile schedules of the persistent kernels (static, one tile per CTA pair,
 dynamic counter) and raster groups give the oracle's results; the dynamic
 schedule also keeps its bounded waits (a skipped load is reported, and the
-next call is correct)."""
+next call is correct), and plans running at once on several streams do not
+disturb each other."""
 import numpy as np
 import pytest
 
@@ -190,3 +191,51 @@ def test_raster_orders_give_the_same_bits(data, kernel):
     assert mask_mismatch(unpack_words(to_host_words(aux), M), z_o)[0] == 0
     assert_close(to_host_f32(dz), oracle.decode(dz_o, 0), what="dZ")
     assert_close(bg.cpu().numpy(), bgrad_o, BGRAD_NMAX, BGRAD_REL, what="bgrad")
+
+
+def test_plans_on_two_streams_at_once():
+    """A forward plan and a backward plan (and a wide-tile forward) enqueued on
+    three streams so that their persistent kernels overlap, several times in
+    a row: each plan's tile counter and status word are its own, so every
+    output is the same bits as when the plans run one after the other."""
+    Mc, Nc, Kc = 4096, 4096, 2048
+    X = to_dev(synth.normal((Mc, Kc), synth.F16, 50, synth.TID_A, 1.0), 0)
+    W = to_dev(synth.normal((Kc, Nc), synth.F16, 50, synth.TID_B, 1 / np.sqrt(Kc)), 0)
+    Wt = to_dev(synth.normal((Nc, Kc), synth.F16, 50, synth.TID_W2, 1 / np.sqrt(Kc)), 0)
+    b = to_dev(synth.normal((Nc,), synth.F16, 50, synth.TID_BIAS, 0.1), 0)
+    words = to_dev(synth.mask_words(Mc, Nc, 50), 0)
+    fwd = gf.gf_matmul_plan(Mc, Nc, Kc, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    gf.gf_plan_set_option(fwd, gf.GF_OPT_KERNEL, 2)
+    wide = gf.gf_matmul_plan(Mc, Nc, Kc, gf.GF_F16, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
+    gf.gf_plan_set_option(wide, gf.GF_OPT_KERNEL, 3)
+    bwd = gf.gf_matmul_plan_ex(Mc, Nc, Kc, gf.GF_F16, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                               gf.GF_B_NK)
+
+    def outs():
+        return (torch.empty((Mc, Nc), dtype=torch.float16, device="cuda"),
+                torch.empty((Mc // 32, Nc), dtype=torch.int32, device="cuda"),
+                torch.empty((Mc, Nc), dtype=torch.float16, device="cuda"),
+                torch.empty((Mc // 32, Nc), dtype=torch.int32, device="cuda"),
+                torch.empty((Mc, Nc), dtype=torch.float16, device="cuda"),
+                torch.empty((Nc,), dtype=torch.float32, device="cuda"))
+
+    def launch(o, streams):
+        s1, s2, s3 = (s.cuda_stream for s in streams)
+        gf.gf_matmul_execute(fwd, X, W, bias=b, out=o[0], aux_out=o[1], stream=s1)
+        gf.gf_matmul_execute(wide, X, W, bias=b, out=o[2], aux_out=o[3], stream=s2)
+        gf.gf_matmul_execute(bwd, X, Wt, out=o[4], aux_in=words, bgrad=o[5], stream=s3)
+
+    cur = torch.cuda.current_stream()
+    ref = outs()
+    launch(ref, (cur, cur, cur))  # one after the other
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    for _ in range(3):
+        o = outs()
+        launch(o, streams)
+        torch.cuda.synchronize()
+        for a, r in zip(o, ref):
+            assert torch.equal(a.view(torch.uint8), r.view(torch.uint8))
+    for p in (fwd, wide, bwd):
+        assert gf.gf_plan_status(p) == gf.GF_OK
+        p.free()
