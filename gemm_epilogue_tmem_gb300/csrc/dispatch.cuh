@@ -31,9 +31,9 @@ cudaError_t launch_instance(const LaunchArgs& a) {
   return cudaLaunchKernelEx(&cfg, kernel, *a.tmA, *a.tmB, *a.tmB2, *a.params);
 }
 
-template <int EPI, typename T, bool B_MN, bool WIDE = false>
+template <int EPI, typename T, bool B_MN, bool WIDE = false, bool SPLITK = false>
 cudaError_t launch_pair_instance(const LaunchArgs& a) {
-  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE>;
+  auto kernel = gemm_epilog_pair_kernel<EPI, T, B_MN, WIDE, SPLITK>;
   using C = PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE),
                     pair_stg(EPI, WIDE), pair_side_ring(EPI, WIDE), pair_stg2(EPI, WIDE)>;
   constexpr int smem = C::kSmemBytes;
@@ -113,6 +113,17 @@ cudaError_t launch_dual(const LaunchArgs& a) {
 
 template <int EPI>
 cudaError_t launch_epi(const LaunchArgs& a) {
+  if (a.pair && a.split) {  // split-k units: 256 x 256 tiles, EPILOG_NONE only
+    if constexpr (EPI == EPI_NONE) {
+      if (a.wide) return cudaErrorInvalidValue;
+      if (a.bf16)
+        return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true, false, true>(a)
+                      : launch_pair_instance<EPI, __nv_bfloat16, false, false, true>(a);
+      return a.b_mn ? launch_pair_instance<EPI, __half, true, false, true>(a)
+                    : launch_pair_instance<EPI, __half, false, false, true>(a);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (a.pair && a.wide) {
     if (a.bf16)
       return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true, true>(a)

@@ -131,7 +131,7 @@ struct PairCfg {
   static constexpr int kSmemBytes = kSmemAlignSlack + kStages * (kABytes + kStageBBytes) +
                                     kCtrlBytes + kRedBytes + kStgBytes;
   static_assert(kStages >= 3 && kSmemBytes <= kSmemPerCta, "shared memory budget");
-  static_assert(16 * kStages + 128 <= kCtrlBytes, "control region");
+  static_assert(16 * kStages + 132 <= kCtrlBytes, "control region");
 };
 
 constexpr int kTileRing = 4;  // tile indices in flight between the roles (dynamic schedule)
@@ -177,7 +177,11 @@ __device__ __forceinline__ void store_aux_words(const GemmParams& p, int row0w, 
   }
 }
 
-template <int EPI, typename T, bool B_MN, bool WIDE = false>
+// SPLITK (256 x 256 tiles, one B operand): the tiles from p.split_from on
+// run as p.k_splits work units of consecutive k-blocks each; a unit's CTAs
+// leave their fp32 partial sums in the workspace, and the last CTA of each
+// rank of a tile to finish adds them in split order and runs the epilogue.
+template <int EPI, typename T, bool B_MN, bool WIDE = false, bool SPLITK = false>
 __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
                                           pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
                                           pair_side_ring(EPI, WIDE),
@@ -191,6 +195,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
   using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
                     pair_side_ring(EPI, WIDE), pair_stg2(EPI, WIDE)>;
+  static_assert(!SPLITK || (!WIDE && NB == 1 && C::kEpiWarps == 4), "split k: 256 x 256 tiles");
   constexpr int kRing = pair_side_ring(EPI, WIDE);
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
@@ -218,6 +223,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   const uint32_t tile_empty0 = ctrl + 16u * S + 80u;  // leader: kTileRing barriers, index read
   const uint32_t ring_s = ctrl + 16u * S + 112u;      // both: kTileRing tile indices
   volatile int* ring = reinterpret_cast<volatile int*>(gctrl + 16 * S + 112);
+  // split k: whether this CTA's epilogue counted last for its tile and rank
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gctrl + 16 * S + 128);
   float* red = reinterpret_cast<float*>(gctrl + C::kCtrlBytes);
   const uint32_t stg0 = ctrl + C::kCtrlBytes + C::kRedBytes;  // 2 KB output staging per warp
   const uint32_t side0 = stg0 + C::kEpiWarps * 2048u;           // wide: 1 KB side inputs per warp
@@ -231,7 +238,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   const bool leader = rank == 0;
   const int cluster_id = blockIdx.x >> 1;
   const int num_clusters = gridDim.x >> 1;
-  const int num_pair_tiles = p.num_tiles;  // the host counts pair tiles for this kernel
+  // work units: the pair tiles (the host counts pair tiles for this kernel),
+  // with split k the split tiles' units in their place
+  const int num_pair_tiles =
+      SPLITK ? p.split_from + (p.num_tiles - p.split_from) * p.k_splits : p.num_tiles;
   const bool dynamic = p.tile_counter != nullptr;
 
   if (threadIdx.x == 0) {
@@ -293,6 +303,19 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
     return t;
   };
 
+  // work unit u -> tile, split (-1: the whole tile) and k-blocks [kb0, kb1)
+  auto unit_tile = [&](int u, int& split, int& kb0, int& kb1) -> int {
+    split = -1;
+    kb0 = 0;
+    kb1 = p.num_k_blocks;
+    if (!SPLITK || u < p.split_from) return u;
+    const int v = u - p.split_from;
+    split = v % p.k_splits;
+    kb0 = split * p.kb_per_split;
+    kb1 = min(p.num_k_blocks, kb0 + p.kb_per_split);
+    return p.split_from + v / p.k_splits;
+  };
+
   if (warp < C::kCtlWarps) {
     // control warps: warpgroup 0 of the wide tiles gives registers to the
     // two epilogue warpgroups (the host checks the launch's register count)
@@ -348,13 +371,15 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           }
         }
         if (t < 0) break;
+        int split, kb0, kb1;
+        if constexpr (SPLITK) t = unit_tile(t, split, kb0, kb1);
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
         const int m_row = mb2 * 256 + 128 * (int)rank;  // this CTA's A rows
         // this CTA's B columns (two operands: the tile's columns of its own
         // operand; wide: part h at n_col + 256 h)
         const int n_col = NB == 2 ? nb * BN : nb * BN + 128 * (int)rank;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = SPLITK ? kb0 : 0; kb < (SPLITK ? kb1 : p.num_k_blocks); ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
             ok = false;
@@ -416,6 +441,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           break;
         }
         if (t < 0) break;
+        int split, kb0, kb1;
+        if constexpr (SPLITK) unit_tile(t, split, kb0, kb1);
         // double buffer: tile it uses buffer it & 1, whose previous use (tile
         // it - 2) must be drained; wide: one buffer in two halves, released
         // by the epilogue of tile it - 1 one after the other
@@ -451,10 +478,10 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
             umma_f16_pair(d_tmem + 256u * (uint32_t)h, adesc, bdesc, idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+                          ((SPLITK ? kb - kb0 : kb) | kk) != 0 ? 1u : 0u);
           }
         };
-        int kb = 0;
+        int kb = SPLITK ? kb0 : 0;
         if constexpr (WIDE) {
           // half 0 over the first stages that the producer has loaded while
           // the previous tile drained, then half 1 of the same stages
@@ -495,7 +522,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         // wide: the last S k-slices go half 0 first, then half 1, so that
         // half 0 is complete (and its drain starts) S k-slices early
         const int tail = WIDE && p.num_k_blocks - kb >= 2 * S ? S : 0;
-        for (; kb < p.num_k_blocks - tail; ++kb) {
+        for (; kb < (SPLITK ? kb1 : p.num_k_blocks) - tail; ++kb) {
           if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
             ok = false;
@@ -579,6 +606,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         break;
       }
       if (t < 0) break;
+      int split, kb0, kb1;
+      if constexpr (SPLITK) t = unit_tile(t, split, kb0, kb1);
       int mb2, nb;
       pair_tile_coords(p, t, mb2, nb);
       const int row0 = mb2 * 256 + 128 * (int)rank;
@@ -683,8 +712,18 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);
       } else {
         constexpr bool kStg = pair_stg(EPI, false);
-        epilogue_drain<EPI, T, BN, BN, kStg, false, kRing>(
-            p, t_row, row0, n0, q, lane, red, stg0 + 2048u * (uint32_t)ew, sring);
+        // split k: this unit's partial sums go to the workspace; the last
+        // CTA of this rank of the tile to count adds all of them, in split
+        // order, into its accumulator and drains it
+        bool drain = true;
+        if constexpr (SPLITK) {
+          if (split >= 0)
+            drain = splitk_reduce<BN>(p, t_row, 2 * (t - p.split_from) + (int)rank, split,
+                                      p.k_splits, q, lane, ep_tid, last_flag, 0u, 0u);
+        }
+        if (drain)
+          epilogue_drain<EPI, T, BN, BN, kStg, false, kRing>(
+              p, t_row, row0, n0, q, lane, red, stg0 + 2048u * (uint32_t)ew, sring);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(tempty_leader + 8u * buf);

@@ -24,6 +24,7 @@ struct LaunchArgs {
   int tile_n;   // 128 or 256 (single-CTA kernel)
   int pair;     // 1: the CTA-pair kernel (256 x 256 tiles)
   int wide;     // with pair: 256 x 512 tiles (one accumulator in two halves)
+  int split;    // with pair: split-k work units (256 x 256 tiles, EPILOG_NONE)
   int pdl;      // 1: programmatic dependent launch (set-up overlaps the previous kernel)
   cudaStream_t stream;
 };

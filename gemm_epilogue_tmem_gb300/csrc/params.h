@@ -86,6 +86,10 @@ struct GemmParams {
   int32_t kb_per_split;
   float* splitk_ws;     // fp32 partial sums [num_tiles][k_splits][tile_n / 4][128] float4
   int32_t* splitk_cnt;  // [num_tiles] splits done per tile; zero between launches
+  // CTA-pair kernel, split k: tiles [0, split_from) run whole, each later
+  // tile as k_splits units of kb_per_split k-blocks; partials and counters
+  // per (split tile, CTA rank): [(t - split_from) * 2 + rank]
+  int32_t split_from;
 };
 
 }  // namespace gf

@@ -53,6 +53,7 @@ struct gf_plan {
   float* d_partials;     // [num_m_blocks][n] fp32, DRELU_BGRAD two-pass only
   size_t partial_bytes;
   int forced_split;      // 0 the plan's choice, 1 no split, else k-splits per tile
+  int split_from;        // CTA-pair split k: the first tile split into k-split units
   int k_splits;          // single-CTA kernel: CTAs sharing the k-blocks of one tile
   int kb_per_split;
   void* d_splitk;        // split-k partial sums, then the per-tile counters
@@ -248,13 +249,49 @@ void plan_tiles(gf_plan* p) {
     p->raster_n = 1;
     if (p->forced_group_m == 0) p->group_m = 4;
   }
+  p->split_from = 0;
   if (pair) {
     p->tile_n = pair_n;
     p->stages = gf::stages_for(pair_n, 1, p->epi);
     p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
-    const int64_t clusters = pair_tiles < p->max_pair_clusters ? pair_tiles : p->max_pair_clusters;
-    p->grid = static_cast<int>(2 * (p->one_tile_per_cta ? pair_tiles : clusters));
+    // Split k on 256 x 256 tiles (EPILOG_NONE): when the tiles fill at most
+    // three waves of the resident pairs and leave the last one at most half
+    // full, the last wave's tiles are shared by several pairs each (k-blocks
+    // in consecutive runs), so that the last wave ends after a fraction of a
+    // tile; the tiles before run whole. GF_OPT_SPLIT_K >= 2 splits every
+    // tile that many ways.
+    int want = 0;
+    int64_t from = 0;
+    const int64_t cl = p->max_pair_clusters;
+    if (!wide && !dual && p->epi == gf::EPI_NONE && p->num_k_blocks >= 2 && cl > 0) {
+      if (p->forced_split >= 2) {
+        want = p->forced_split;
+      } else if (p->forced_split == 0 && p->num_k_blocks >= 32) {
+        const int64_t full = pair_tiles / cl * cl;
+        const int64_t rem = pair_tiles - full;
+        if (rem > 0 && pair_tiles <= 3 * cl && 2 * rem <= cl) {
+          int64_t w = cl / rem;
+          if (w > 8) w = 8;
+          if (w > p->num_k_blocks / 8) w = p->num_k_blocks / 8;
+          want = static_cast<int>(w);
+          from = full;
+        }
+      }
+    }
+    if (want >= 2) {
+      const int kps = (p->num_k_blocks + want - 1) / want;
+      const int ks = (p->num_k_blocks + kps - 1) / kps;  // every split gets k-blocks
+      const size_t ws = static_cast<size_t>(pair_tiles - from) * 2 * ks * kBM * pair_n * 4;
+      if (ks >= 2 && ws <= kMaxSplitkBytes) {
+        p->k_splits = ks;
+        p->kb_per_split = kps;
+        p->split_from = static_cast<int>(from);
+      }
+    }
+    const int64_t units = p->split_from + (pair_tiles - p->split_from) * p->k_splits;
+    const int64_t clusters = units < p->max_pair_clusters ? units : p->max_pair_clusters;
+    p->grid = static_cast<int>(2 * (p->one_tile_per_cta ? units : clusters));
     return;
   }
   int tn = p->forced_tile_n;
@@ -308,8 +345,11 @@ void plan_tiles(gf_plan* p) {
 // too small; on failure the plan falls back to no split.
 gf_status ensure_splitk(gf_plan* p) {
   if (p->k_splits < 2) return GF_OK;
-  const size_t ws = static_cast<size_t>(p->num_tiles) * p->k_splits * kBM * p->tile_n * 4;
-  const size_t need = ws + static_cast<size_t>(p->num_tiles) * 4;
+  // partial sums per split tile, or per (split tile, CTA rank) for the pair kernel
+  const size_t parts = p->pair ? 2 * static_cast<size_t>(p->num_tiles - p->split_from)
+                               : static_cast<size_t>(p->num_tiles);
+  const size_t ws = parts * p->k_splits * kBM * p->tile_n * 4;
+  const size_t need = ws + parts * 4;
   gf_status st = GF_OK;
   if (need > p->splitk_bytes) {
     if (p->d_splitk) cudaFree(p->d_splitk);
@@ -322,8 +362,7 @@ gf_status ensure_splitk(gf_plan* p) {
   }
   if (st == GF_OK) {
     p->splitk_cnt_offset = ws;
-    if (cudaMemset(static_cast<char*>(p->d_splitk) + ws, 0, static_cast<size_t>(p->num_tiles) * 4) !=
-        cudaSuccess)
+    if (cudaMemset(static_cast<char*>(p->d_splitk) + ws, 0, parts * 4) != cudaSuccess)
       st = GF_ERR_CUDA;
   }
   if (st != GF_OK) {
@@ -606,6 +645,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   prm.l2_hint_b = p->l2_hint_b;
   prm.b_mn_3d = b_mn_3d ? 1 : 0;
   if (p->k_splits > 1) {
+    prm.split_from = p->split_from;
     prm.k_splits = p->k_splits;
     prm.kb_per_split = p->kb_per_split;
     prm.splitk_ws = static_cast<float*>(p->d_splitk);
@@ -640,6 +680,7 @@ gf_status execute_impl(const gf_plan* p, const ExecArgs& x, cudaStream_t st) {
   la.tile_n = p->tile_n;
   la.pair = p->pair;
   la.wide = p->wide;
+  la.split = p->pair && p->k_splits > 1 ? 1 : 0;
   la.pdl = p->pdl;
   la.stream = st;
 
@@ -926,9 +967,11 @@ GF_API gf_status gf_plan_status(const gf_plan* p, struct CUstream_st* stream) {
     // which gave up may leave part-way
     if (cudaMemset(p->d_status, 0, 256) != cudaSuccess) return fail(GF_ERR_CUDA);
     // a launch that gave up may leave split-k counters part-way
+    const size_t counters = p->pair ? 2 * static_cast<size_t>(p->num_tiles - p->split_from)
+                                    : static_cast<size_t>(p->num_tiles);
     if (p->k_splits > 1 &&
-        cudaMemset(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset, 0,
-                   static_cast<size_t>(p->num_tiles) * 4) != cudaSuccess)
+        cudaMemset(static_cast<char*>(p->d_splitk) + p->splitk_cnt_offset, 0, counters * 4) !=
+            cudaSuccess)
       return fail(GF_ERR_CUDA);
     return fail(GF_ERR_DEVICE_TIMEOUT);
   }

@@ -260,3 +260,70 @@ def test_autotune_keeps_a_correct_split():
     plan.free()
     y_o, _ = oracle.relu_bias(A, B, bias, 0, axis=oracle.BIAS_ROW)
     assert_close(to_host_f32(out), oracle.decode(y_o, 0), what="Y after autotune")
+
+
+# ----------------------------------------------------------- CTA-pair kernel
+def _pair_plan(M, N, K, dtype, layout, split):
+    plan = gf.gf_matmul_plan_ex(M, N, K, dtype, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL, layout)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SPLIT_K, split)
+    d = gf.gf_plan_describe(plan)
+    assert (d["tile_m"], d["tile_n"]) == (256, 256), d
+    return plan
+
+
+@pytest.mark.parametrize("M,N,K", [(1000, 1032, 1000), (512, 2568, 4104), (300, 264, 520)])
+@pytest.mark.parametrize("layout", [gf.GF_B_KN, gf.GF_B_NK])
+@pytest.mark.parametrize("split", [2, 3, 8])
+def test_pair_split_every_tile(M, N, K, layout, split):
+    """256 x 256 CTA-pair tiles with every tile split k ways (a ragged last
+    split, rows and columns past M and N): against the oracle, twice in a row
+    (the per-tile counters are back at zero after each launch), the same bits
+    both times."""
+    d = synth.BF16
+    A, B, _ = _fwd_inputs(M, N, K, d, layout, 71, gf.GF_BIAS_COL)
+    plan = _pair_plan(M, N, K, d, layout, split)
+    assert gf.gf_plan_describe(plan)["k_splits"] == _expected_splits(K, split)
+    Ad, Bd = to_dev(A, d), to_dev(B, d)
+    outs = []
+    for _ in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        gf.gf_matmul_execute(plan, Ad, Bd, out=out)
+        assert gf.gf_plan_status(plan) == gf.GF_OK
+        outs.append(out)
+    plan.free()
+    ob = oracle.B_KN if layout == gf.GF_B_KN else oracle.B_NK
+    assert_close(to_host_f32(outs[0]), oracle.decode(oracle.epilog_none(A, B, d, ob), d),
+                 what="NONE, pair split")
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_pair_split_last_wave_plan_choice():
+    """The plan's own choice on a product whose 256 x 256 tiles fill two waves
+    of the resident CTA pairs and leave 3 tiles for a third: those are split
+    (the tiles before run whole), and the result matches the oracle on
+    sampled rows."""
+    d = synth.BF16
+    big = gf.gf_matmul_plan_ex(4096, 8192, 128, d, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL, gf.GF_B_NK)
+    gf.gf_plan_set_option(big, gf.GF_OPT_KERNEL, 2)
+    pairs = gf.gf_plan_describe(big)["grid"] // 2  # 512 tiles: every resident pair
+    big.free()
+    M, K = 256, 2048
+    N = 256 * (2 * pairs + 3)
+    A = synth.normal((M, K), d, 72, synth.TID_A, 1.0)
+    B = synth.normal((N, K), d, 72, synth.TID_B, 1 / np.sqrt(K))
+    plan = gf.gf_matmul_plan_ex(M, N, K, d, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL, gf.GF_B_NK)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_KERNEL, 2)
+    ks = gf.gf_plan_describe(plan)["k_splits"]
+    assert 2 <= ks <= 8, ks
+    outs = []
+    for _ in range(2):
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        gf.gf_matmul_execute(plan, to_dev(A, d), to_dev(B, d), out=out)
+        assert gf.gf_plan_status(plan) == gf.GF_OK
+        outs.append(out)
+    plan.free()
+    rows = synth.sample_rows(M, 32, 72)
+    o_rows = oracle.decode(oracle.epilog_none(A[rows], B, d, oracle.B_NK), d)
+    assert_close(to_host_f32(outs[0])[rows], o_rows, what="NONE, plan's split")
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
