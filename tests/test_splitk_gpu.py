@@ -5,7 +5,9 @@ ragged shapes (a k tail in the last split, rows and columns past M and N),
 both B layouts and tile widths, more work units than SMs, bit-for-bit
 repeatability across launches, guard zones around every output, the
 time-out path and the plan's own choice on the (1024, 512, 2048) row-bias
-GEMM."""
+GEMM. The CTA-pair kernel's split (256 x 256 tiles, EPILOG_NONE): every tile
+split, and the plan's split of a mostly empty last wave, against the
+oracle."""
 import numpy as np
 import pytest
 
@@ -327,3 +329,28 @@ def test_pair_split_last_wave_plan_choice():
     o_rows = oracle.decode(oracle.epilog_none(A[rows], B, d, oracle.B_NK), d)
     assert_close(to_host_f32(outs[0])[rows], o_rows, what="NONE, plan's split")
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_pair_split_swiglu_down_shape():
+    """The SwiGLU MLP's down projection at M = 2048 (h[2048, 17408] ·
+    Wdᵀ, Wd stored [5120, 17408]): 160 tiles of 256 x 256 fill two waves of
+    the resident CTA pairs and leave a few tiles over, which the plan splits;
+    32 sampled rows against the oracle."""
+    d = synth.BF16
+    M, N, K = 2048, 5120, 17408
+    h = synth.normal((M, K), d, 73, synth.TID_A, 1.0)
+    Wd = synth.normal((N, K), d, 73, synth.TID_WD, 0.02)
+    plan = gf.gf_matmul_plan_ex(M, N, K, d, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL, gf.GF_B_NK)
+    desc = gf.gf_plan_describe(plan)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    gf.gf_matmul_execute(plan, to_dev(h, d), to_dev(Wd, d), out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    # the documented rule: at most three waves, the last one at most half full
+    pairs, tiles = desc["grid"] // 2, 160
+    rem = tiles % pairs
+    if desc["tile_n"] == 256 and rem and tiles <= 3 * pairs and 2 * rem <= pairs:
+        assert desc["k_splits"] >= 2, desc
+    rows = synth.sample_rows(M, 32, 73)
+    o_rows = oracle.decode(oracle.epilog_none(h[rows], Wd, d, oracle.B_NK), d)
+    assert_close(to_host_f32(out)[rows], o_rows, what="down projection")
