@@ -462,6 +462,9 @@ def run_gpu(args):
     bwd_none = gf.gf_matmul_plan_ex(M, K, N, gf.GF_F16, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL,
                                     gf.GF_B_NK)
     launches_per_step = 3  # fused forward, fused backward, bgrad finalize
+    # the bare GEMMs without a k split, as the fused plans run
+    for pl in (fwd_none, bwd_none):
+        gf.gf_plan_set_option(pl, gf.GF_OPT_SPLIT_K, 1)
     if args.kernel:
         for pl in (fwd, bwd, fwd_none, bwd_none):
             gf.gf_plan_set_option(pl, gf.GF_OPT_KERNEL, args.kernel)
@@ -765,6 +768,8 @@ def run_profile_case(args):
         gf.gf_plan_set_option(plan, gf.GF_OPT_L2_HINTS, args.l2_hints)
     if args.group_m:
         gf.gf_plan_set_option(plan, gf.GF_OPT_GROUP_M, args.group_m)
+    if args.split:
+        gf.gf_plan_set_option(plan, gf.GF_OPT_SPLIT_K, args.split)
     for _ in range(args.warmup + args.steps):
         if epi == gf.GF_EPILOG_DRELU_BGRAD:
             gf.gf_matmul_execute(plan, A, B, out=out, aux_in=aux, bgrad=bgrad, stream=sp)
@@ -1012,8 +1017,10 @@ def run_gelu_workload(args, gf, torch, dev, sp, pk, pk_kind):
         "bwd_none": gf.gf_matmul_plan_ex(Mg, Kg, Ng, gf.GF_BF16, gf.GF_EPILOG_NONE,
                                          gf.GF_BIAS_COL, gf.GF_B_NK),
     }
-    # the bare GEMMs run in the fused plans' kernel and tile configuration
+    # the bare GEMMs run in the fused plans' kernel and tile configuration,
+    # without a k split
     for a, b in (("fwd_none", "fwd"), ("bwd_none", "bwd")):
+        gf.gf_plan_set_option(plan[a], gf.GF_OPT_SPLIT_K, 1)
         d = gf.gf_plan_describe(plan[b])
         kern = (3 if d["tile_n"] == 512 else 2) if d["tile_m"] == 256 else 1
         gf.gf_plan_set_option(plan[a], gf.GF_OPT_KERNEL, kern)
@@ -1150,8 +1157,10 @@ def run_swiglu_workload(args, gf, torch, dev, sp, pk, pk_kind, Ms):
                                        gf.GF_B_KN)
         # the bare GEMMs run in the fused plans' kernel and tile configuration
         # (the gate+up kernel's tiles are half as wide as the bare GEMM's of
-        # [Wg; Wu]: each output column takes a column of both operands)
+        # [Wg; Wu]: each output column takes a column of both operands),
+        # without a k split
         for a, b, wide_n in ((bare, fwd, 256), (dh_none, bwd, 512)):
+            gf.gf_plan_set_option(a, gf.GF_OPT_SPLIT_K, 1)
             d = gf.gf_plan_describe(b)
             kern = (3 if d["tile_n"] == wide_n else 2) if d["tile_m"] == 256 else 1
             gf.gf_plan_set_option(a, gf.GF_OPT_KERNEL, kern)
@@ -1553,6 +1562,9 @@ def main():
                     help="--profile-case: GF_OPT_L2_HINTS of the plan (-1: the plan's default)")
     ap.add_argument("--group-m", type=int, default=0,
                     help="--profile-case: GF_OPT_GROUP_M of the plan (0: the plan's default)")
+    ap.add_argument("--split", type=int, default=0,
+                    help="--profile-case: GF_OPT_SPLIT_K of the plan (0: the plan's choice, "
+                         "1: none)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)

@@ -113,9 +113,15 @@ cudaError_t launch_dual(const LaunchArgs& a) {
 
 template <int EPI>
 cudaError_t launch_epi(const LaunchArgs& a) {
-  if (a.pair && a.split) {  // split-k units: 256 x 256 tiles, EPILOG_NONE only
+  if (a.pair && a.split) {  // split-k units: EPILOG_NONE only
     if constexpr (EPI == EPI_NONE) {
-      if (a.wide) return cudaErrorInvalidValue;
+      if (a.wide) {
+        if (a.bf16)
+          return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true, true, true>(a)
+                        : launch_pair_instance<EPI, __nv_bfloat16, false, true, true>(a);
+        return a.b_mn ? launch_pair_instance<EPI, __half, true, true, true>(a)
+                      : launch_pair_instance<EPI, __half, false, true, true>(a);
+      }
       if (a.bf16)
         return a.b_mn ? launch_pair_instance<EPI, __nv_bfloat16, true, false, true>(a)
                       : launch_pair_instance<EPI, __nv_bfloat16, false, false, true>(a);

@@ -826,21 +826,29 @@ __device__ __forceinline__ void epilogue_bgrad(const GemmParams& p, const float*
 // workspace and counts itself in the tile's counter; the CTA that counts last
 // adds the partials in split order -- the sum does not depend on which split
 // finishes last -- writes it back into its accumulator and runs the epilogue.
-// No CTA waits for another. Returns true in that last CTA. Called by the 128
-// epilogue threads (ep_tid 0..127, thread = accumulator row 32 q + lane).
+// No CTA waits for another. Returns true in that last CTA. Called by the NT
+// epilogue threads (ep_tid 0..NT-1, thread = accumulator row 32 q + lane).
+// With NT = 128 a thread takes the whole row; with 256 (two warps per lane
+// quarter) the row's BN / 2 columns of this warp, in segments of SEG columns
+// SEG_STRIDE apart from column c_off.
 // A partial is stored as [BN / 4][128 rows] float4 pieces, so that the 32
 // lanes of a warp (32 consecutive rows) move 512 contiguous bytes per access.
-template <int BN>
+template <int BN, int NT = 128, int SEG = BN, int SEG_STRIDE = BN>
 __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_row, int t, int s,
                                               int ks, int q, uint32_t lane, int ep_tid,
                                               volatile int* last_flag, uint32_t ring,
-                                              uint32_t ring_bytes) {
+                                              uint32_t ring_bytes, int c_off = 0) {
   constexpr int kPart = kBM * BN / 4;  // float4 pieces of one partial
+  constexpr int kCols = BN * kBM / NT;  // columns of one thread
+  static_assert(kCols % SEG == 0 && SEG % 32 == 0, "whole 32-column chunks");
+  // accumulator column of this thread's column i (i a multiple of 32)
+  auto col_of = [&](int i) { return c_off + (i / SEG) * SEG_STRIDE + i % SEG; };
   const int row = 32 * q + static_cast<int>(lane);
   float4* tile_ws = reinterpret_cast<float4*>(p.splitk_ws) + static_cast<size_t>(t) * ks * kPart;
   float4* mine = tile_ws + static_cast<size_t>(s) * kPart + row;
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
+  for (int i = 0; i < kCols; i += 32) {
+    const int c = col_of(i);
     uint32_t v[32];
     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), v);
     tmem_ld_wait_tied(v);
@@ -851,22 +859,22 @@ __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_ro
                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
   }
   __threadfence();
-  named_bar_sync(1, 128);
+  named_bar_sync(1, NT);
   if (ep_tid == 0) {
     const int done = atomicAdd(p.splitk_cnt + t, 1);
     const int last = done == ks - 1 ? 1 : 0;
     if (last) p.splitk_cnt[t] = 0;  // every split has counted: ready for the next launch
     *last_flag = last;
   }
-  named_bar_sync(1, 128);
+  named_bar_sync(1, NT);
   if (*last_flag == 0) return false;
   __threadfence();
   // When the operand ring is idle (`ring_bytes` > 0: this CTA's last unit,
   // every stage consumed) and holds the other splits' partials, they come in
   // by asynchronous copies all issued at once -- piece pc of this row from
   // the j-th other split at ((j * BN / 4 + pc) * 128 + row) * 16 -- instead
-  // of a few loads in flight per thread.
-  const bool staged = ring_bytes >= static_cast<uint32_t>((ks - 1) * kPart * 16);
+  // of a few loads in flight per thread (whole rows: NT = 128 only).
+  const bool staged = NT == 128 && ring_bytes >= static_cast<uint32_t>((ks - 1) * kPart * 16);
   if (staged) {
     int j = 0;
 #pragma unroll 1
@@ -883,7 +891,8 @@ __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_ro
     cp_async_wait_all();  // each thread reads back only what it copied itself
   }
 #pragma unroll 1
-  for (int c = 0; c < BN; c += 32) {
+  for (int i = 0; i < kCols; i += 32) {
+    const int c = col_of(i);
     // this CTA's own partial is still in its accumulator
     uint32_t own[32];
     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c), own);
@@ -913,13 +922,16 @@ __device__ __forceinline__ bool splitk_reduce(const GemmParams& p, uint32_t t_ro
         for (int i = 0; i < 32; ++i) acc[i] = sp == 0 ? x[i] : acc[i] + x[i];
       }
     } else {
+      // (two splits' pieces in flight at once with whole rows; one with the
+      // 256-thread form, whose threads hold more live state)
+      constexpr int kStep = NT == 128 ? 2 : 1;
 #pragma unroll 1
-      for (int sp = 0; sp < ks; sp += 2) {
-        // two splits' pieces in flight at once; a split's own piece from TMEM
+      for (int sp = 0; sp < ks; sp += kStep) {
+        // a split's own piece from TMEM
         float4 x[8], y[8];
         const float4* a = src + static_cast<size_t>(sp) * kPart;
         const float4* b = a + kPart;
-        const bool has_b = sp + 1 < ks;
+        const bool has_b = kStep == 2 && sp + 1 < ks;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           x[j] = sp == s ? make_float4(__uint_as_float(own[4 * j]), __uint_as_float(own[4 * j + 1]),

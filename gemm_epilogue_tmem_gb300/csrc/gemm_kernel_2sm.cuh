@@ -177,10 +177,11 @@ __device__ __forceinline__ void store_aux_words(const GemmParams& p, int row0w, 
   }
 }
 
-// SPLITK (256 x 256 tiles, one B operand): the tiles from p.split_from on
-// run as p.k_splits work units of consecutive k-blocks each; a unit's CTAs
-// leave their fp32 partial sums in the workspace, and the last CTA of each
-// rank of a tile to finish adds them in split order and runs the epilogue.
+// SPLITK (256 x 256 or wide tiles, one B operand): the tiles from
+// p.split_from on run as p.k_splits work units of consecutive k-blocks each;
+// a unit's CTAs leave their fp32 partial sums in the workspace, and the last
+// CTA of each rank of a tile to finish adds them in split order and runs the
+// epilogue.
 template <int EPI, typename T, bool B_MN, bool WIDE = false, bool SPLITK = false>
 __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(EPI), WIDE,
                                           pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
   constexpr int NB = epi_dual(EPI) ? 2 : 1;
   using C = PairCfg<NB, epi_has_bgrad(EPI), WIDE, pair_epi8(EPI, WIDE), pair_stg(EPI, WIDE),
                     pair_side_ring(EPI, WIDE), pair_stg2(EPI, WIDE)>;
-  static_assert(!SPLITK || (!WIDE && NB == 1 && C::kEpiWarps == 4), "split k: 256 x 256 tiles");
+  static_assert(!SPLITK || (NB == 1 && (WIDE || C::kEpiWarps == 4)),
+                "split k: one B operand, 256 x 256 or wide tiles");
   constexpr int kRing = pair_side_ring(EPI, WIDE);
   constexpr int S = C::kStages;
   constexpr int BN = C::BN;
@@ -481,11 +483,14 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
                           ((SPLITK ? kb - kb0 : kb) | kk) != 0 ? 1u : 0u);
           }
         };
-        int kb = SPLITK ? kb0 : 0;
+        // this unit's k-blocks
+        const int kbeg = SPLITK ? kb0 : 0;
+        const int kend = SPLITK ? kb1 : p.num_k_blocks;
+        int kb = kbeg;
         if constexpr (WIDE) {
           // half 0 over the first stages that the producer has loaded while
           // the previous tile drained, then half 1 of the same stages
-          const int pre = p.num_k_blocks < S ? p.num_k_blocks : S;
+          const int pre = kend - kbeg < S ? kend - kbeg : S;
           int st = stage;
           uint32_t ph = phase;
           for (int j = 0; j < pre && ok; ++j) {
@@ -496,7 +501,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
               break;
             }
             tc_fence_after();
-            mma_kslice(st, j, 0);
+            mma_kslice(st, kbeg + j, 0);
             if (++st == S) {
               st = 0;
               ph ^= 1u;
@@ -510,19 +515,19 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           }
           tc_fence_after();
           for (int j = 0; j < pre; ++j) {
-            mma_kslice(stage, j, 1);
+            mma_kslice(stage, kbeg + j, 1);
             umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          kb = pre;
+          kb = kbeg + pre;
         }
         // wide: the last S k-slices go half 0 first, then half 1, so that
         // half 0 is complete (and its drain starts) S k-slices early
-        const int tail = WIDE && p.num_k_blocks - kb >= 2 * S ? S : 0;
-        for (; kb < (SPLITK ? kb1 : p.num_k_blocks) - tail; ++kb) {
+        const int tail = WIDE && kend - kb >= 2 * S ? S : 0;
+        for (; kb < kend - tail; ++kb) {
           if (!mbar_wait_bounded(full0 + 8u * stage, phase, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_MMA_SMEM);
             ok = false;
@@ -599,7 +604,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         if (lane == 0) mbar_arrive_remote(tile_empty_leader + 8u * (it % kTileRing));
       }
       bool ok = t != -2;
-      if constexpr (epi_has_bgrad(EPI)) ok = !named_bar_red_or(1, NT, !ok);
+      // (the epilogs with a barrier of all epilogue warps agree on the outcome)
+      if constexpr (epi_has_bgrad(EPI) || SPLITK) ok = !named_bar_red_or(1, NT, !ok);
       if (!ok) {
         raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
         aborted = true;
@@ -628,10 +634,11 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
       const int buf = WIDE ? 0 : (it & 1);
       const uint32_t use = WIDE ? (uint32_t)it & 1u : (uint32_t)(it >> 1) & 1u;
       // the accumulator (wide: accumulator half h) is complete; all epilogue
-      // warps take part (the bias-gradient epilogs agree on the outcome)
+      // warps take part (the bias-gradient and split-k epilogs agree on the
+      // outcome)
       auto wait_acc = [&](uint32_t h) -> bool {
         bool okh = mbar_wait_bounded(tfull0 + 8u * (buf + h), use, abort_flag, p.wait_limit_ns);
-        if constexpr (epi_has_bgrad(EPI)) okh = !named_bar_red_or(1, NT, !okh);
+        if constexpr (epi_has_bgrad(EPI) || SPLITK) okh = !named_bar_red_or(1, NT, !okh);
         if (okh) tc_fence_after();
         return okh;
       };
@@ -681,6 +688,26 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             break;
           }
         } else {
+          if constexpr (SPLITK) {
+            if (split >= 0) {
+              // split k: both halves complete, this unit's partial sums go to
+              // the workspace; the last CTA of this rank of the tile to count
+              // adds all of them, in split order, into its accumulator and
+              // drains it, the others release both halves
+              if (!wait_acc(0u) || !wait_acc(1u)) {
+                raise_error(p, abort_flag, ST_TIMEOUT_EPILOGUE);
+                aborted = true;
+                break;
+              }
+              if (!splitk_reduce<BN, NT, 128, 256>(p, t_row, 2 * (t - p.split_from) + (int)rank,
+                                                   split, p.k_splits, q, lane, ep_tid, last_flag,
+                                                   0u, 0u, c_sub)) {
+                release_half(0u);
+                release_half(1u);
+                continue;
+              }
+            }
+          }
           if (!epilogue_drain<EPI, T, 128, BN, true, kSide, 0, true, true>(
                   p, t_row + (uint32_t)c_sub, row0, n0 + c_sub, q, lane, red + c_sub, stg, side,
                   &tmOut, &tmAux, &aw, [&]() { release_half(0u); }, stg2,

@@ -255,22 +255,21 @@ void plan_tiles(gf_plan* p) {
     p->stages = gf::stages_for(pair_n, 1, p->epi);
     p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
-    // Split k on 256 x 256 tiles (EPILOG_NONE): when the tiles fill at most
-    // three waves of the resident pairs and leave the last one at most half
-    // full, the last wave's tiles are shared by several pairs each (k-blocks
-    // in consecutive runs), so that the last wave ends after a fraction of a
-    // tile; the tiles before run whole. GF_OPT_SPLIT_K >= 2 splits every
-    // tile that many ways.
+    // Split k (EPILOG_NONE, 256 x 256 or wide tiles): when the tiles leave
+    // the last wave of the resident pairs at most half full, that wave's
+    // tiles are shared by several pairs each (k-blocks in consecutive runs),
+    // so that it ends after a fraction of a tile; the tiles before run
+    // whole. GF_OPT_SPLIT_K >= 2 splits every tile that many ways.
     int want = 0;
     int64_t from = 0;
     const int64_t cl = p->max_pair_clusters;
-    if (!wide && !dual && p->epi == gf::EPI_NONE && p->num_k_blocks >= 2 && cl > 0) {
+    if (!dual && p->epi == gf::EPI_NONE && p->num_k_blocks >= 2 && cl > 0) {
       if (p->forced_split >= 2) {
         want = p->forced_split;
       } else if (p->forced_split == 0 && p->num_k_blocks >= 32) {
         const int64_t full = pair_tiles / cl * cl;
         const int64_t rem = pair_tiles - full;
-        if (rem > 0 && pair_tiles <= 3 * cl && 2 * rem <= cl) {
+        if (rem > 0 && 2 * rem <= cl) {
           int64_t w = cl / rem;
           if (w > 8) w = 8;
           if (w > p->num_k_blocks / 8) w = p->num_k_blocks / 8;

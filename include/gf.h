@@ -280,11 +280,11 @@ typedef enum gf_option {
  * tiles); 1..4096 otherwise. */
 /* GF_OPT_SPLIT_K: the single-CTA kernel shares the k-blocks of each output
  * tile among this many CTAs (one B operand only); so does the CTA-pair kernel
- * with 256 x 256 tiles for GF_EPILOG_NONE plans (each of its CTAs then has a
- * partial sum and a counter of its own, and the last to finish for its 128
- * rows adds them; the plan's choice there splits only the tiles of a last
- * wave that is at most half full, when the tiles fill at most three waves
- * and k has at least 32 blocks).
+ * with 256 x 256 or 256 x 512 tiles for GF_EPILOG_NONE plans (each of its
+ * CTAs then has a partial sum and a counter of its own, and the last to
+ * finish for its 128 rows adds them; the plan's choice there splits only the
+ * tiles of a last wave that is at most half full, when k has at least 32
+ * blocks).
  * Each CTA leaves its fp32 partial sum in the plan's workspace; the last one
  * of a tile to finish adds the partials in split order (the result does not
  * depend on which finishes last) and runs the epilogue, so no CTA waits for
