@@ -228,9 +228,33 @@ void plan_tiles(gf_plan* p) {
   const int64_t tiles256 = m2 * ((p->n + pair_n_narrow - 1) / pair_n_narrow);
   const int64_t tiles512 = m2 * ((p->n + pair_n_wide - 1) / pair_n_wide);
   const int64_t cl = p->max_pair_clusters > 0 ? p->max_pair_clusters : 1;
+  // The plan's split k of the CTA-pair tiles (EPILOG_NONE): when `tiles`
+  // leave the last wave of the resident pairs at most half full, that
+  // wave's tiles are shared by several pairs each (k-blocks in consecutive
+  // runs), so that it ends after a fraction of a tile; the tiles before run
+  // whole. Beyond three waves the tiles' own spread in time already fills
+  // part of the last wave, and the split paid only on long tiles (k >= 8192:
+  // measured on the SwiGLU down GEMM; at k = 4096 over 13 waves it gave
+  // nothing). Returns the splits, or 0.
+  auto last_wave_split = [&](int64_t tiles) -> int {
+    if (dual || p->epi != gf::EPI_NONE || p->forced_split != 0 || p->max_pair_clusters <= 0)
+      return 0;
+    const int64_t rem = tiles % cl;
+    if (rem == 0 || 2 * rem > cl || p->num_k_blocks < (tiles <= 3 * cl ? 32 : 128)) return 0;
+    int64_t w = cl / rem;
+    if (w > 8) w = 8;
+    if (w > p->num_k_blocks / 8) w = p->num_k_blocks / 8;
+    return w >= 2 ? static_cast<int>(w) : 0;
+  };
+  // the time of `tiles` in eighths of a tile's time per pair
+  auto eighths = [&](int64_t tiles) -> int64_t {
+    const int w = last_wave_split(tiles);
+    const int64_t full = tiles / cl;
+    return 8 * full + (tiles == full * cl ? 0 : w ? (8 + w - 1) / w : 8);
+  };
   const bool wide_fits = p->max_pair_clusters > 0;
-  const bool wide_pays = wide_fits && p->k >= 2048 &&
-                         100 * 2 * ((tiles512 + cl - 1) / cl) <= 112 * ((tiles256 + cl - 1) / cl);
+  const bool wide_pays =
+      wide_fits && p->k >= 2048 && 100 * 2 * eighths(tiles512) <= 112 * eighths(tiles256);
   const bool wide = wide_fits && (p->forced_kernel == 3 || (p->forced_kernel == 0 && wide_pays));
   const int pair_n = wide ? pair_n_wide : pair_n_narrow;
   const int64_t pair_tiles = wide ? tiles512 : tiles256;
@@ -255,27 +279,17 @@ void plan_tiles(gf_plan* p) {
     p->stages = gf::stages_for(pair_n, 1, p->epi);
     p->num_n_blocks = static_cast<int>((p->n + pair_n - 1) / pair_n);
     p->num_tiles = static_cast<int>(pair_tiles);
-    // Split k (EPILOG_NONE, 256 x 256 or wide tiles): when the tiles leave
-    // the last wave of the resident pairs at most half full, that wave's
-    // tiles are shared by several pairs each (k-blocks in consecutive runs),
-    // so that it ends after a fraction of a tile; the tiles before run
-    // whole. GF_OPT_SPLIT_K >= 2 splits every tile that many ways.
+    // Split k (EPILOG_NONE, 256 x 256 or wide tiles): the plan's split of
+    // a last wave (above); GF_OPT_SPLIT_K >= 2 splits every tile that many
+    // ways.
     int want = 0;
     int64_t from = 0;
-    const int64_t cl = p->max_pair_clusters;
-    if (!dual && p->epi == gf::EPI_NONE && p->num_k_blocks >= 2 && cl > 0) {
+    if (!dual && p->epi == gf::EPI_NONE && p->num_k_blocks >= 2) {
       if (p->forced_split >= 2) {
         want = p->forced_split;
-      } else if (p->forced_split == 0 && p->num_k_blocks >= 32) {
-        const int64_t full = pair_tiles / cl * cl;
-        const int64_t rem = pair_tiles - full;
-        if (rem > 0 && 2 * rem <= cl) {
-          int64_t w = cl / rem;
-          if (w > 8) w = 8;
-          if (w > p->num_k_blocks / 8) w = p->num_k_blocks / 8;
-          want = static_cast<int>(w);
-          from = full;
-        }
+      } else {
+        want = last_wave_split(pair_tiles);
+        from = pair_tiles / cl * cl;
       }
     }
     if (want >= 2) {

@@ -284,7 +284,8 @@ typedef enum gf_option {
  * CTAs then has a partial sum and a counter of its own, and the last to
  * finish for its 128 rows adds them; the plan's choice there splits only the
  * tiles of a last wave that is at most half full, when k has at least 32
- * blocks).
+ * blocks, or 128 when the tiles fill more than three waves, and it takes the
+ * 256 x 512 tiles when their split schedule is the shorter one).
  * Each CTA leaves its fp32 partial sum in the plan's workspace; the last one
  * of a tile to finish adds the partials in split order (the result does not
  * depend on which finishes last) and runs the epilogue, so no CTA waits for

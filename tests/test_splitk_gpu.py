@@ -336,10 +336,10 @@ def test_pair_split_last_wave_plan_choice():
 @pytest.mark.parametrize("M", [2048, 8192])
 def test_pair_split_swiglu_down_shape(M):
     """The SwiGLU MLP's down projection (h[M, 17408] · Wdᵀ, Wd stored
-    [5120, 17408]): at M = 2048 160 tiles of 256 x 256 fill two waves of the
-    resident CTA pairs and leave a few tiles over, at M = 8192 320 tiles of
-    256 x 512 fill four and leave a few; the plan splits those; 32 sampled
-    rows against the oracle."""
+    [5120, 17408]): at M = 2048 80 tiles of 256 x 512 fill one wave of the
+    resident CTA pairs and leave a few tiles over, at M = 8192 320 fill four
+    and leave a few; the plan splits those; 32 sampled rows against the
+    oracle."""
     d = synth.BF16
     N, K = 5120, 17408
     h = synth.normal((M, K), d, 73, synth.TID_A, 1.0)
@@ -350,7 +350,8 @@ def test_pair_split_swiglu_down_shape(M):
     gf.gf_matmul_execute(plan, to_dev(h, d), to_dev(Wd, d), out=out)
     assert gf.gf_plan_status(plan) == gf.GF_OK
     plan.free()
-    # the documented rule: a last wave at most half full
+    # the documented rule: a last wave at most half full, k >= 128 blocks
+    # beyond three waves (here 272 blocks)
     pairs = desc["grid"] // 2
     tiles = (M // 256) * -(-N // desc["tile_n"])
     rem = tiles % pairs
