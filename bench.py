@@ -1167,6 +1167,9 @@ def run_swiglu_workload(args, gf, torch, dev, sp, pk, pk_kind, Ms):
             if d["tile_m"] != 256:
                 gf.gf_plan_set_option(a, gf.GF_OPT_TILE_N, d["tile_n"])
         plans = (fwd, down, bwd, bare, dh_none)
+        plan_desc = {"gate_up_swiglu": gf.gf_plan_describe(fwd),
+                     "down_none": gf.gf_plan_describe(down),
+                     "dh_dswiglu": gf.gf_plan_describe(bwd)}
 
         def t_gateup():
             gt = torch.matmul(x, Wg.t())
@@ -1236,6 +1239,7 @@ def run_swiglu_workload(args, gf, torch, dev, sp, pk, pk_kind, Ms):
             "value": v, "ms_per_step": step, "steps": args.steps, "warmup": args.warmup,
             "pct_of_peak": {"value": 100 * v / peak, "peak_tflops": peak, "peak_kind": peak_src},
             "kernels_ms": tl["per_kernel"],
+            "plans": plan_desc,
             "roofline": _roofline(tl["per_kernel"], flops, peak, peak_src),
             "parity": parity,
             "cpu_baseline": {"value": len(rows) / Mw * (f_gu + 2 * f_mm) / cpu_s / 1e12,
