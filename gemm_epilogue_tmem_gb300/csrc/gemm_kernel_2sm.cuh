@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           }
         }
         if (t < 0) break;
-        int split, kb0, kb1;
+        // this unit's k-blocks [kb0, kb1) (the whole k of a whole tile)
+        int split = -1, kb0 = 0, kb1 = p.num_k_blocks;
         if constexpr (SPLITK) t = unit_tile(t, split, kb0, kb1);
         int mb2, nb;
         pair_tile_coords(p, t, mb2, nb);
@@ -381,7 +382,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         // this CTA's B columns (two operands: the tile's columns of its own
         // operand; wide: part h at n_col + 256 h)
         const int n_col = NB == 2 ? nb * BN : nb * BN + 128 * (int)rank;
-        for (int kb = SPLITK ? kb0 : 0; kb < (SPLITK ? kb1 : p.num_k_blocks); ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(empty0 + 8u * stage, phase ^ 1u, abort_flag, p.wait_limit_ns)) {
             raise_error(p, abort_flag, ST_TIMEOUT_PRODUCER);
             ok = false;
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
           break;
         }
         if (t < 0) break;
-        int split, kb0, kb1;
+        int split = -1, kb0 = 0, kb1 = p.num_k_blocks;
         if constexpr (SPLITK) unit_tile(t, split, kb0, kb1);
         // double buffer: tile it uses buffer it & 1, whose previous use (tile
         // it - 2) must be drained; wide: one buffer in two halves, released
@@ -480,12 +481,12 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
             const uint64_t bdesc = B_MN ? sdesc_sw128(b_base + kk * 2048, 64 * kBK * 2, 1024)
                                         : sdesc_sw128(b_base + kk * 32, 16, 1024);
             umma_f16_pair(d_tmem + 256u * (uint32_t)h, adesc, bdesc, idesc,
-                          ((SPLITK ? kb - kb0 : kb) | kk) != 0 ? 1u : 0u);
+                          ((kb - kb0) | kk) != 0 ? 1u : 0u);
           }
         };
         // this unit's k-blocks
-        const int kbeg = SPLITK ? kb0 : 0;
-        const int kend = SPLITK ? kb1 : p.num_k_blocks;
+        const int kbeg = kb0;
+        const int kend = kb1;
         int kb = kbeg;
         if constexpr (WIDE) {
           // half 0 over the first stages that the producer has loaded while
@@ -612,7 +613,7 @@ __global__ void __launch_bounds__(PairCfg<epi_dual(EPI) ? 2 : 1, epi_has_bgrad(E
         break;
       }
       if (t < 0) break;
-      int split, kb0, kb1;
+      int split = -1, kb0 = 0, kb1 = p.num_k_blocks;
       if constexpr (SPLITK) t = unit_tile(t, split, kb0, kb1);
       int mb2, nb;
       pair_tile_coords(p, t, mb2, nb);
