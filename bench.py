@@ -409,13 +409,41 @@ def run_e2e(args, gf, torch, fwd, bwd, dev, world, barrier, dev_in0, dev_out0):
     barrier()
     ms = t0.elapsed_time(t1) / n
     ok = gf.gf_plan_status(fwd, sc) == gf.GF_OK and gf.gf_plan_status(bwd, sc) == gf.GF_OK
+
+    # what bounds it: one step's copies with no kernels running, each
+    # direction alone and both at once (median of 3)
+    def copies(dirs):
+        out = []
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s_h2d)
+            s_d2h.wait_stream(s_h2d)
+            if "in" in dirs:
+                with torch.cuda.stream(s_h2d):
+                    for k, t in dev_in[0].items():
+                        t.copy_(host_in[k], non_blocking=True)
+            if "out" in dirs:
+                with torch.cuda.stream(s_d2h):
+                    for k, t in dev_out[0].items():
+                        host_out[0][k].copy_(t, non_blocking=True)
+            s_h2d.wait_stream(s_d2h)
+            b.record(s_h2d)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+        return sorted(out)[1]
+    c_in, c_out, c_both = copies(("in",)), copies(("out",)), copies(("in", "out"))
+    link = {"h2d_alone_ms": c_in, "d2h_alone_ms": c_out, "both_at_once_ms": c_both,
+            "h2d_gbs": h2d / (c_in * 1e-3) / 1e9, "d2h_gbs": d2h / (c_out * 1e-3) / 1e9,
+            "note": "one step's copies with no kernels running: the step cannot be shorter "
+                    "than both_at_once_ms or than the kernels"}
     del host_in, host_out, dev_in, dev_out
     torch.cuda.empty_cache()
     return {"value": world * 2 * FLOP_PER_GEMM / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "ms_per_step": ms, "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "H2D of step i+1 and D2H of step i-1 on their own streams under step i; "
                        "the timed region includes the first step's H2D and the last step's D2H",
-            "status_ok": ok}
+            "host_link": link, "status_ok": ok}
 
 
 # ------------------------------------------------------------------- GPU leg
