@@ -302,6 +302,33 @@ def test_pair_split_every_tile(M, N, K, layout, split, kernel):
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
 
 
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_pair_split_timeout_then_reuse(kernel):
+    """The CTA-pair kernel with every tile split: each CTA skips a stage load,
+    the bounded waits run out (the epilogue warps agree on it before any
+    barrier of the hand-over), the host reads GF_ERR_DEVICE_TIMEOUT and resets
+    the per-tile counters left part-way, and the next launch of the same plan
+    matches the oracle."""
+    d = synth.BF16
+    M, N, K = 512, 1024, 2048
+    A, B, _ = _fwd_inputs(M, N, K, d, gf.GF_B_NK, 74, gf.GF_BIAS_COL)
+    Ad, Bd = to_dev(A, d), to_dev(B, d)
+    plan = _pair_plan(M, N, K, d, gf.GF_B_NK, 2, kernel)
+    assert gf.gf_plan_describe(plan)["k_splits"] == 2
+    gf.gf_plan_set_option(plan, gf.GF_OPT_WAIT_LIMIT_US, 20000)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 3)
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    gf.gf_matmul_execute(plan, Ad, Bd, out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_ERR_DEVICE_TIMEOUT
+    gf.gf_plan_set_option(plan, gf.GF_OPT_FAULT_DROP_LOAD, 0)
+    out.fill_(float("nan"))
+    gf.gf_matmul_execute(plan, Ad, Bd, out=out)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    assert_close(to_host_f32(out), oracle.decode(oracle.epilog_none(A, B, d, oracle.B_NK), d),
+                 what="NONE after the time-out")
+
+
 def test_pair_split_last_wave_plan_choice():
     """The plan's own choice on a product whose 256 x 256 tiles fill two waves
     of the resident CTA pairs and leave 3 tiles for a third: those are split
