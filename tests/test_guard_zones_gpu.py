@@ -5,7 +5,8 @@ relu_aux words, a saved activation, the bias gradient) is placed between two
 selects the 3-D or the 2-D B loads) the guards must be untouched and the
 outputs must match the oracle. Covers the single-CTA kernel (128- and
 256-wide tiles), the CTA pair (256 x 256) and the wide pair (256 x 512), with
-direct and staged (shared-memory transposed) stores."""
+direct and staged (shared-memory transposed) stores, and each form's split-k
+hand-over."""
 import numpy as np
 import pytest
 
@@ -116,7 +117,7 @@ def test_guards_gelu_aux_bias(kernel, tile_n):
     assert_close(to_host_f32(aux.view.view(M, N)), oracle.decode(aux_o, d), what="pre-activation")
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_guards_swiglu_save(kernel):
     M, I, H = 1000, 776, 200
     d = synth.BF16
@@ -155,3 +156,26 @@ def test_guards_dswiglu(kernel):
     dg_o, du_o, _ = oracle.dswiglu_backward(dout, Wd, g, u, d)
     assert_close(to_host_f32(dg.view.view(M, I)), oracle.decode(dg_o, d), what="d_gate")
     assert_close(to_host_f32(du.view.view(M, I)), oracle.decode(du_o, d), what="d_up")
+
+
+@pytest.mark.parametrize("kernel,tile_n", KERNELS)
+@pytest.mark.parametrize("N", [776, 832])
+def test_guards_split_k(kernel, tile_n, N):
+    """Every tile's k split 3 ways (a ragged last split): the partial sums go
+    through the plan's workspace and only the output's own elements are
+    written."""
+    M, K = 1000, 1000
+    d = synth.BF16
+    A = synth.normal((M, K), d, 65, synth.TID_A, 1.0)
+    B = synth.normal((K, N), d, 65, synth.TID_B, 1 / np.sqrt(K))
+    out = Guarded(M * N, torch.bfloat16)
+    plan = gf.gf_matmul_plan_ex(M, N, K, d, gf.GF_EPILOG_NONE, gf.GF_BIAS_COL, gf.GF_B_KN)
+    _set(plan, kernel, tile_n)
+    gf.gf_plan_set_option(plan, gf.GF_OPT_SPLIT_K, 3)
+    assert gf.gf_plan_describe(plan)["k_splits"] == 3
+    gf.gf_matmul_execute(plan, to_dev(A, d), to_dev(B, d), out=out.view)
+    assert gf.gf_plan_status(plan) == gf.GF_OK
+    plan.free()
+    assert out.intact()
+    assert_close(to_host_f32(out.view.view(M, N)), oracle.decode(oracle.epilog_none(A, B, d), d),
+                 what="NONE, split k")
