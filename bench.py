@@ -352,36 +352,39 @@ def run_reference(args):
 def run_e2e(args, gf, torch, fwd, bwd, dev, world, barrier, dev_in0, dev_out0):
     """The step through the C ABI from pinned host memory: every step copies
     its inputs host -> device, runs the fused forward and backward, and copies
-    every output device -> host. Copies of step i+1 / i-1 run on their own
-    streams under the compute of step i (two buffer sets), the way a training
-    or serving loop would overlap them."""
+    every output device -> host. Copies of later / earlier steps run on their
+    own streams under the compute of step i (`--e2e-depth` buffer sets), the
+    way a training or serving loop would overlap them."""
+    depth = max(2, args.e2e_depth)
     host_in = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in dev_in0.items()}
     for n, t in dev_in0.items():
         host_in[n].copy_(t)
     host_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                 for n, t in dev_out0.items()} for _ in range(2)]
-    dev_in = [dev_in0, {n: torch.empty_like(t) for n, t in dev_in0.items()}]
-    dev_out = [dev_out0, {n: torch.empty_like(t) for n, t in dev_out0.items()}]
+                 for n, t in dev_out0.items()} for _ in range(depth)]
+    dev_in = [dev_in0] + [{n: torch.empty_like(t) for n, t in dev_in0.items()}
+                          for _ in range(depth - 1)]
+    dev_out = [dev_out0] + [{n: torch.empty_like(t) for n, t in dev_out0.items()}
+                            for _ in range(depth - 1)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     s_comp = torch.cuda.current_stream(dev)
     sc = s_comp.cuda_stream
-    h2d_done = [torch.cuda.Event() for _ in range(2)]
-    comp_done = [torch.cuda.Event() for _ in range(2)]
-    d2h_done = [torch.cuda.Event() for _ in range(2)]
+    h2d_done = [torch.cuda.Event() for _ in range(depth)]
+    comp_done = [torch.cuda.Event() for _ in range(depth)]
+    d2h_done = [torch.cuda.Event() for _ in range(depth)]
 
     def run(n):
         for i in range(n):
-            b = i % 2
-            if i >= 2:
+            b = i % depth
+            if i >= depth:  # buffer set b is free once step i - depth is done with it
                 s_h2d.wait_event(comp_done[b])
             with torch.cuda.stream(s_h2d):
                 for k, t in dev_in[b].items():
                     t.copy_(host_in[k], non_blocking=True)
             h2d_done[b].record(s_h2d)
             s_comp.wait_event(h2d_done[b])
-            if i >= 2:
+            if i >= depth:
                 s_comp.wait_event(d2h_done[b])
             di, do = dev_in[b], dev_out[b]
             gf.gf_matmul_execute(fwd, di["X"], di["W"], bias=di["bias"], out=do["Y"],
@@ -395,7 +398,7 @@ def run_e2e(args, gf, torch, fwd, bwd, dev, world, barrier, dev_in0, dev_out0):
                     host_out[b][k].copy_(t, non_blocking=True)
             d2h_done[b].record(s_d2h)
 
-    run(2)
+    run(depth)
     barrier()
     # enough steps that the pipeline's fill (the first step's copy in) and
     # drain (the last step's copy out) are a small share of the timed region
@@ -404,7 +407,7 @@ def run_e2e(args, gf, torch, fwd, bwd, dev, world, barrier, dev_in0, dev_out0):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s_h2d)
     run(n)
-    s_d2h.wait_event(d2h_done[(n - 1) % 2])
+    s_d2h.wait_event(d2h_done[(n - 1) % depth])
     t1.record(s_d2h)
     barrier()
     ms = t0.elapsed_time(t1) / n
@@ -441,8 +444,9 @@ def run_e2e(args, gf, torch, fwd, bwd, dev, world, barrier, dev_in0, dev_out0):
     torch.cuda.empty_cache()
     return {"value": world * 2 * FLOP_PER_GEMM / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "ms_per_step": ms, "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "overlap": "H2D of step i+1 and D2H of step i-1 on their own streams under step i; "
-                       "the timed region includes the first step's H2D and the last step's D2H",
+            "overlap": f"{depth} buffer sets: H2D of later steps and D2H of earlier steps on "
+                       "their own streams under step i; the timed region includes the first "
+                       "step's H2D and the last step's D2H",
             "host_link": link, "status_ok": ok}
 
 
@@ -1606,6 +1610,9 @@ def main():
     ap.add_argument("--ref-step-rows", type=int, default=4,
                     help="sampled rows per GEMM in each step of --impl reference")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-depth", type=int, default=2,
+                    help="buffer sets of the e2e pipeline (inputs and outputs of that many "
+                         "steps in flight)")
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
