@@ -88,6 +88,8 @@ def lib(path: str | None = None):
         L.gf_plan_describe.argtypes = [_P, _P, _P, _P, _P, _P]
         L.gf_plan_k_splits.restype = _I32
         L.gf_plan_k_splits.argtypes = [_P, _P]
+        L.gf_plan_launches.restype = _I32
+        L.gf_plan_launches.argtypes = [_P, _P]
         L.gf_plan_free.restype = None
         L.gf_plan_free.argtypes = [_P]
         L.gf_status_string.restype = ctypes.c_char_p
@@ -246,8 +248,13 @@ def gf_plan_describe(plan: Plan) -> dict:
     rc = lib().gf_plan_k_splits(plan.handle, ctypes.byref(ks))
     if rc != GF_OK:
         raise GfError(rc, "gf_plan_k_splits")
+    nl = ctypes.c_int32()
+    rc = lib().gf_plan_launches(plan.handle, ctypes.byref(nl))
+    if rc != GF_OK:
+        raise GfError(rc, "gf_plan_launches")
     return {"tile_m": vals[0].value, "tile_n": vals[1].value, "stages": vals[2].value,
-            "grid": vals[3].value, "workspace_bytes": ws.value, "k_splits": ks.value}
+            "grid": vals[3].value, "workspace_bytes": ws.value, "k_splits": ks.value,
+            "launches": nl.value}
 
 
 def gf_plan_free(plan: Plan) -> None:

@@ -934,6 +934,13 @@ GF_API gf_status gf_plan_describe(const gf_plan* p, int32_t* tile_m, int32_t* ti
   return GF_OK;
 }
 
+GF_API gf_status gf_plan_launches(const gf_plan* p, int32_t* launches) {
+  if (!p || !launches) return fail(GF_ERR_INVALID_VALUE);
+  const bool finalize = has_bgrad(p->epi) && p->bgrad_mode != GF_BGRAD_ATOMIC;
+  *launches = p->m == 0 || p->n == 0 ? 0 : 1 + (finalize ? 1 : 0);
+  return GF_OK;
+}
+
 GF_API gf_status gf_plan_k_splits(const gf_plan* p, int32_t* k_splits) {
   if (!p || !k_splits) return fail(GF_ERR_INVALID_VALUE);
   *k_splits = p->k_splits;

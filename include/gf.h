@@ -339,6 +339,13 @@ GF_API gf_status gf_plan_describe(const gf_plan* plan, int32_t* tile_m, int32_t*
  * NULL argument. */
 GF_API gf_status gf_plan_k_splits(const gf_plan* plan, int32_t* k_splits);
 
+/* The number of kernels one execute of the plan enqueues in its current
+ * configuration: 0 for an empty output, else 1, plus 1 for the bias-gradient
+ * epilogs in GF_BGRAD_TWO_PASS mode (the finalize kernel that adds the
+ * partials; GF_BGRAD_ATOMIC enqueues a memset of bgrad instead).
+ * GF_ERR_INVALID_VALUE for a NULL argument. */
+GF_API gf_status gf_plan_launches(const gf_plan* plan, int32_t* launches);
+
 /*
  * DRELU_BGRAD that allocates nothing. The pages have no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc (or any

@@ -69,6 +69,8 @@ def test_null_plan_calls(L):
     ks = ctypes.c_int32(-1)
     assert L.gf_plan_k_splits(None, ctypes.byref(ks)) == gf.GF_ERR_INVALID_VALUE
     assert ks.value == -1
+    assert L.gf_plan_launches(None, ctypes.byref(ks)) == gf.GF_ERR_INVALID_VALUE
+    assert ks.value == -1
     L.gf_plan_free(None)
 
 

@@ -276,9 +276,10 @@ def _kernel_nodes(graph_handle: int) -> int:
 
 
 def test_one_fused_launch():
-    """One execute = one kernel launch (plus the bgrad finalize for the
-    two-pass backward). Counted from a CUDA graph capture of execute (the
-    SwiGLU sample counts launches too, so that "1 kernel" is shown:
+    """One execute = one kernel launch, plus the bgrad finalize for the
+    two-pass backward (single-CTA and CTA-pair kernels). Counted from a CUDA
+    graph capture of execute, and equal to what gf_plan_launches reports
+    (the SwiGLU sample counts launches too, so that "1 kernel" is shown:
     gemm_swiglu_mlp_fusion.py, ``_demo``)."""
     M, N, K = 512, 512, 256
     A = torch.randn((M, K), device="cuda").half()
@@ -290,9 +291,14 @@ def test_one_fused_launch():
     bgrad = torch.empty(N, dtype=torch.float32, device="cuda")
     fwd = gf.gf_matmul_plan(M, N, K, 0, gf.GF_EPILOG_RELU_AUX_BIAS, gf.GF_BIAS_COL)
     bwd = gf.gf_matmul_plan_ex(M, N, K, 0, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL, gf.GF_B_NK)
-    counts = []
+    bwd_pair = gf.gf_matmul_plan_ex(M, N, K, 0, gf.GF_EPILOG_DRELU_BGRAD, gf.GF_BIAS_COL,
+                                    gf.GF_B_NK)
+    gf.gf_plan_set_option(bwd_pair, gf.GF_OPT_KERNEL, 2)
+    counts, declared = [], []
     for plan, kw in ((fwd, dict(bias=bias, out=out, aux_out=aux)),
-                     (bwd, dict(out=out, aux_in=mask, bgrad=bgrad))):
+                     (bwd, dict(out=out, aux_in=mask, bgrad=bgrad)),
+                     (bwd_pair, dict(out=out, aux_in=mask, bgrad=bgrad))):
+        declared.append(gf.gf_plan_describe(plan)["launches"])
         gf.gf_matmul_execute(plan, A, B, **kw)
         torch.cuda.synchronize()
         ref = out.clone()
@@ -306,9 +312,10 @@ def test_one_fused_launch():
         g.replay()  # the captured launch replays to the same result
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
-    assert counts == [1, 2], counts
+    assert counts == [1, 2, 2] and declared == counts, (counts, declared)
     fwd.free()
     bwd.free()
+    bwd_pair.free()
 
 
 def test_dependent_launch_changes_nothing():
