@@ -252,9 +252,13 @@ void plan_tiles(gf_plan* p) {
     const int64_t full = tiles / cl;
     return 8 * full + (tiles == full * cl ? 0 : w ? (8 + w - 1) / w : 8);
   };
+  // (two B operands: the wide tile saves less -- 1-3 % at the power cap on
+  // the SwiGLU gate+up, where the 256 x 128 tile was 1.2 % faster at
+  // M = 2048, 8 against 15 waves)
   const bool wide_fits = p->max_pair_clusters > 0;
+  const int64_t wide_gain = dual ? 104 : 112;
   const bool wide_pays =
-      wide_fits && p->k >= 2048 && 100 * 2 * eighths(tiles512) <= 112 * eighths(tiles256);
+      wide_fits && p->k >= 2048 && 100 * 2 * eighths(tiles512) <= wide_gain * eighths(tiles256);
   const bool wide = wide_fits && (p->forced_kernel == 3 || (p->forced_kernel == 0 && wide_pays));
   const int pair_n = wide ? pair_n_wide : pair_n_narrow;
   const int64_t pair_tiles = wide ? tiles512 : tiles256;
