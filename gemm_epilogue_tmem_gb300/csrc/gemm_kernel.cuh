@@ -104,17 +104,28 @@ __device__ __forceinline__ float tanh_fast(float x) {
 }
 
 // tanh form of GELU (Hendrycks & Gimpel, "Gaussian Error Linear Units",
-// 2016): 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))), and its derivative.
+// 2016): 0.5 z (1 + tanh(c (z + k z^3))) with c = sqrt(2/pi), k = 0.044715,
+// and its derivative 0.5 (1 + t) + 0.5 z (1 - t^2) c (1 + 3 k z^2), t the
+// tanh. Written as u = z (c + c k z^2) and 0.5 z + 0.5 z t, in fused
+// multiply-adds with c k and 3 c k folded: five operations and one tanh per
+// element for the forward, nine and one for the derivative.
+constexpr float kGeluC = 0.7978845608028654f;     // sqrt(2 / pi)
+constexpr float kGeluCK = 0.035677408136300125f;  // sqrt(2 / pi) * 0.044715
+constexpr float kGelu3CK = 0.10703222440890038f;  // 3 sqrt(2 / pi) * 0.044715
+
 __device__ __forceinline__ float gelu_tanh(float z) {
-  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
-  return 0.5f * z * (1.f + tanh_fast(u));
+  const float z2 = z * z;
+  const float u = z * fmaf(kGeluCK, z2, kGeluC);
+  const float h = 0.5f * z;
+  return fmaf(h, tanh_fast(u), h);
 }
 
 __device__ __forceinline__ float dgelu_tanh(float z) {
-  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
-  const float t = tanh_fast(u);
-  return 0.5f * (1.f + t) +
-         0.5f * z * (1.f - t * t) * 0.7978845608028654f * (1.f + 3.f * 0.044715f * z * z);
+  const float z2 = z * z;
+  const float t = tanh_fast(z * fmaf(kGeluCK, z2, kGeluC));
+  const float b = fmaf(kGelu3CK, z2, kGeluC);  // c (1 + 3 k z^2)
+  const float s = fmaf(-t, t, 1.f);            // 1 - t^2
+  return fmaf(0.5f * z * s, b, fmaf(0.5f, t, 0.5f));
 }
 
 // SiLU and the logistic function of the SwiGLU epilogues (gate+up
