@@ -234,8 +234,12 @@ GF_API gf_status gf_plan_status(const gf_plan* plan, struct CUstream_st* stream)
  *                          GF_ERR_DEVICE_TIMEOUT from gf_plan_status. 0: off.
  * GF_OPT_KERNEL          : 0 the plan's choice (the CTA-pair kernel when its
  *                          256-row tiles fill the resident pairs, with
- *                          256 x 512 tiles when k >= 2048 and their waves
- *                          quantise no worse; else the single-CTA kernel),
+ *                          256 x 512 tiles when k >= 2048 and their
+ *                          schedule -- waves of the resident pairs, with the
+ *                          last-wave split of GF_OPT_SPLIT_K -- is no longer
+ *                          than the 256 x 256 tiles' weighed by the wide
+ *                          tile's gain, 12 % (4 % for the gate+up SwiGLU
+ *                          plans); else the single-CTA kernel),
  *                          1 the single-CTA kernel
  *                          (128 x tile_n tiles), 2 the CTA-pair kernel
  *                          (256 x 256 tiles on two SMs, 256 x 128 for the
